@@ -1,0 +1,257 @@
+// api.cu -- the C ABI of libattn.so: argument checks, planning and dispatch.
+//
+// Every entry point validates its arguments on the host, resolves the
+// defaults (scale = float nearest 1/sqrt(head_dim), causal offset
+// k_len - q_len: "Attention" (recursiveai.org OneGPU docs), section "What it
+// covers"), picks a kernel from the dtype, head_dim and layout, and enqueues
+// it on the caller's stream.  Nothing here allocates device memory or
+// synchronises, except attn_device_status.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "prefill_tc.h"
+#include "decode.h"
+
+namespace attn {
+
+// Sticky device status word: a kernel that gives up a bounded wait stores
+// ATTN_ERR_DEVICE_TIMEOUT here; attn_device_status reads and clears it.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+
+int status_ptr(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
+size_t elem_size(int32_t dt) { return dt == ATTN_F32 ? 4 : 2; }
+
+bool layout_ok(const attn_layout& l) {
+  return l.offset >= 0 && l.batch_stride >= 0 && l.head_stride >= 0 && l.row_stride >= 0;
+}
+
+bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+// Checks the scalar fields; returns ATTN_OK or an error code.
+int check_problem(const attn_problem* p) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->heads < 1 || p->kv_heads < 1 || p->q_len < 0 || p->k_len < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->heads % p->kv_heads) return ATTN_ERR_INVALID_ARG;
+  if (p->head_dim < 1 || p->head_dim > 256) return ATTN_ERR_INVALID_ARG;
+  if (p->dtype != ATTN_F32 && p->dtype != ATTN_F16 && p->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (p->dtype != ATTN_F32 && (p->head_dim & 1)) return ATTN_ERR_INVALID_ARG;  // half needs an even head_dim
+  if (p->causal != 0 && p->causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (p->masked_rows != ATTN_MASKED_ROWS_NAN && p->masked_rows != ATTN_MASKED_ROWS_ZERO)
+    return ATTN_ERR_INVALID_ARG;
+  if (!(p->scale == p->scale) || isinf(p->scale)) return ATTN_ERR_INVALID_ARG;
+  if (!layout_ok(p->q) || !layout_ok(p->k) || !layout_ok(p->v) || !layout_ok(p->o) || !layout_ok(p->mask))
+    return ATTN_ERR_INVALID_ARG;
+  if (p->seg_batch_stride < 0 || p->lse_batch_stride < 0 || p->lse_head_stride < 0) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+Problem resolve(const attn_problem* p, const void* q, const void* k, const void* v, void* o, const float* mask,
+                const int32_t* seg, const int32_t* k_lens, float* lse, int* status) {
+  Problem r;
+  memset(&r, 0, sizeof r);
+  r.B = p->batch;
+  r.H = p->heads;
+  r.G = p->kv_heads;
+  r.Sq = p->q_len;
+  r.Sk = p->k_len;
+  r.D = p->head_dim;
+  r.qpg = p->heads / p->kv_heads;
+  r.dtype = p->dtype;
+  r.scale = p->scale != 0.0f ? p->scale : (float)(1.0 / sqrt((double)p->head_dim));
+  r.causal = p->causal;
+  r.coff = p->causal_offset == ATTN_OFFSET_DEFAULT ? (int64_t)p->k_len - p->q_len : p->causal_offset;
+  r.masked_zero = p->masked_rows == ATTN_MASKED_ROWS_ZERO;
+  r.q = {p->q.offset, p->q.batch_stride, p->q.head_stride, p->q.row_stride};
+  r.k = {p->k.offset, p->k.batch_stride, p->k.head_stride, p->k.row_stride};
+  r.v = {p->v.offset, p->v.batch_stride, p->v.head_stride, p->v.row_stride};
+  r.o = {p->o.offset, p->o.batch_stride, p->o.head_stride, p->o.row_stride};
+  r.m = {p->mask.offset, p->mask.batch_stride, p->mask.head_stride, p->mask.row_stride};
+  r.seg_bs = p->seg_batch_stride;
+  r.lse_bs = p->lse_batch_stride;
+  r.lse_hs = p->lse_head_stride;
+  r.Q = q;
+  r.K = k;
+  r.V = v;
+  r.O = o;
+  r.M = mask;
+  r.seg = seg;
+  r.klens = k_lens;
+  r.lse = lse;
+  r.status = status;
+  return r;
+}
+
+int check_pointers(const attn_problem* p, const void* q, const void* k, const void* v, const void* o,
+                   const float* mask, const int32_t* seg, const int32_t* k_lens, const float* lse) {
+  const size_t es = elem_size(p->dtype);
+  if (!q || !o) return ATTN_ERR_INVALID_ARG;
+  if (p->k_len > 0 && (!k || !v)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, es) || !aligned(o, es) || (k && !aligned(k, es)) || (v && !aligned(v, es)))
+    return ATTN_ERR_ALIGNMENT;
+  if ((mask && !aligned(mask, 4)) || (seg && !aligned(seg, 4)) || (k_lens && !aligned(k_lens, 4)) ||
+      (lse && !aligned(lse, 4)))
+    return ATTN_ERR_ALIGNMENT;
+  return ATTN_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Decode key-range plan: depends only on the shape.  Ranges are a multiple
+// of 32 keys, at least 128 keys, at most 16 of them ("Attention", section
+// "Accuracy at long key lengths"); a range of 512 keys or more is kept
+// whole when the (batch, kv head) pairs alone fill the GPU several times.
+void decode_plan(const attn_problem* p, int* n_splits, int* split_len) {
+  const int64_t Sk = p->k_len > 0 ? p->k_len : 1;
+  int64_t len = (Sk + 15) / 16;
+  len = (len + 31) / 32 * 32;
+  if (len < 128) len = 128;
+  if (len > Sk) len = (Sk + 31) / 32 * 32;
+  *split_len = (int)len;
+  *n_splits = (int)((Sk + len - 1) / len);
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t decode_ws_bytes(const attn_problem* p, int n_splits) {
+  const size_t rows = (size_t)p->batch * p->heads * p->q_len;
+  return round256(rows * n_splits * p->head_dim * sizeof(float)) + round256(rows * n_splits * sizeof(float));
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+size_t attn_fwd_workspace_size(const attn_problem* p) {
+  if (check_problem(p) != ATTN_OK) return 0;
+  return 0;
+}
+
+int attn_fwd(const attn_problem* p, const void* q, const void* k, const void* v, void* o, const float* mask,
+             const int32_t* seg, const int32_t* k_lens, float* lse, void* workspace, size_t workspace_bytes,
+             attn_stream stream) {
+  int rc = check_problem(p);
+  if (rc) return rc;
+  if (p->batch == 0 || p->q_len == 0) return ATTN_OK;
+  rc = check_pointers(p, q, k, v, o, mask, seg, k_lens, lse);
+  if (rc) return rc;
+  (void)workspace;
+  (void)workspace_bytes;
+  int* status = nullptr;
+  rc = status_ptr(&status);
+  if (rc) return rc;
+  Problem r = resolve(p, q, k, v, o, mask, seg, k_lens, lse, status);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int used = 0;
+  rc = prefill_tc_try(r, st, &used);
+  if (rc || used) return rc;
+  Split s{1, p->k_len > 0 ? p->k_len : 1, nullptr, nullptr};
+  return from_cuda(launch_simt(r, s, st));
+}
+
+size_t attn_decode_workspace_size(const attn_problem* p) {
+  if (check_problem(p) != ATTN_OK || p->q_len != 1) return 0;
+  int n = 1, len = 1;
+  decode_plan(p, &n, &len);
+  return decode_ws_bytes(p, n);
+}
+
+int attn_decode(const attn_problem* p, const void* q, const void* k_cache, const void* v_cache, void* o,
+                const float* mask, const int32_t* seg, const int32_t* k_lens, float* lse, void* workspace,
+                size_t workspace_bytes, attn_stream stream) {
+  int rc = check_problem(p);
+  if (rc) return rc;
+  if (p->q_len != 1) return ATTN_ERR_INVALID_ARG;
+  if (p->batch == 0) return ATTN_OK;
+  rc = check_pointers(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse);
+  if (rc) return rc;
+  int n_splits = 1, split_len = 1;
+  decode_plan(p, &n_splits, &split_len);
+  const size_t need = decode_ws_bytes(p, n_splits);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  rc = status_ptr(&status);
+  if (rc) return rc;
+  Problem r = resolve(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse, status);
+  const size_t rows = (size_t)p->batch * p->heads;
+  Split s;
+  s.n_splits = n_splits;
+  s.split_len = split_len;
+  s.part_o = static_cast<float*>(workspace);
+  s.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        round256(rows * n_splits * p->head_dim * sizeof(float)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int used = 0;
+  rc = decode_fast_try(r, s, st, &used);
+  if (rc) return rc;
+  if (!used) {
+    rc = from_cuda(launch_simt(r, s, st));
+    if (rc) return rc;
+  }
+  return from_cuda(launch_combine(r, s, p->dtype, st));
+}
+
+int attn_combine(int32_t n_splits, int32_t rows, int32_t head_dim, const float* part_o, const float* part_lse,
+                 int32_t out_dtype, void* o, int64_t o_row_stride, float* lse, int32_t masked_rows,
+                 attn_stream stream) {
+  if (n_splits < 0 || rows < 0 || head_dim < 1 || head_dim > 256 || o_row_stride < 0) return ATTN_ERR_INVALID_ARG;
+  if (out_dtype != ATTN_F32 && out_dtype != ATTN_F16 && out_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (masked_rows != ATTN_MASKED_ROWS_NAN && masked_rows != ATTN_MASKED_ROWS_ZERO) return ATTN_ERR_INVALID_ARG;
+  if (rows == 0) return ATTN_OK;
+  if (!o || (n_splits > 0 && (!part_o || !part_lse))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(o, elem_size(out_dtype)) || (part_o && !aligned(part_o, 4)) || (part_lse && !aligned(part_lse, 4)) ||
+      (lse && !aligned(lse, 4)))
+    return ATTN_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return from_cuda(launch_combine_flat(n_splits, rows, head_dim, part_o, part_lse, out_dtype, o, o_row_stride, lse,
+                                       masked_rows == ATTN_MASKED_ROWS_ZERO, st));
+}
+
+int attn_device_status(attn_stream stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int* ptr = nullptr;
+  if (status_ptr(&ptr)) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof v) != cudaSuccess) return ATTN_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+  return v == 0 ? ATTN_OK : v;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported combination";
+    case ATTN_ERR_ALIGNMENT: return "misaligned pointer";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// common.cuh -- types shared by the kernels and the host planner of libattn.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+namespace attn {
+
+struct Layout {
+  int64_t off, bs, hs, rs;  // elements: offset, batch, head, row strides
+};
+
+// A validated problem with defaults resolved, passed by value to kernels.
+struct Problem {
+  int B, H, G, Sq, Sk, D, qpg;   // qpg = heads / kv_heads
+  int dtype;                     // ATTN_F32 / ATTN_F16 / ATTN_BF16
+  float scale;
+  int causal;
+  int64_t coff;                  // causal offset (resolved)
+  int masked_zero;
+  Layout q, k, v, o, m;
+  int64_t seg_bs, lse_bs, lse_hs;
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  const float* M;
+  const int32_t* seg;
+  const int32_t* klens;
+  float* lse;
+  int* status;                   // device status word (ATTN_ERR_DEVICE_TIMEOUT on a given-up wait)
+};
+
+// Key range [k_begin, k_end) cut out of [0, Sk) for split passes, and where the
+// per-range partial results go.
+struct Split {
+  int n_splits;      // 1 = no split: write O / LSE directly
+  int split_len;     // keys per range (multiple of 32)
+  float* part_o;     // [rows][n_splits][D], rows = B*H*Sq in (b, h, i) order
+  float* part_lse;   // [rows][n_splits]
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__host__ __device__ __forceinline__ int64_t clamp64(int64_t x, int64_t lo, int64_t hi) {
+  return x < lo ? lo : (x > hi ? hi : x);
+}
+
+// Visible key range [lo, hi) of query row i of batch entry b: the three
+// structural rules (key length, causal bound, segment start) intersect to one
+// interval.
+__device__ __forceinline__ void row_range(const Problem& p, int b, int i, int64_t& lo, int64_t& hi) {
+  hi = p.Sk;
+  if (p.klens) hi = clamp64((int64_t)p.klens[b], 0, p.Sk);
+  if (p.causal) {
+    int64_t c = (int64_t)i + p.coff + 1;
+    hi = c < hi ? c : hi;
+    if (hi < 0) hi = 0;
+  }
+  lo = 0;
+  if (p.seg) lo = clamp64((int64_t)p.seg[(int64_t)b * p.seg_bs + i], 0, p.Sk);
+}
+
+// Host-side launchers (defined in the kernel translation units).
+cudaError_t launch_simt(const Problem& p, const Split& s, cudaStream_t st);
+cudaError_t launch_combine(const Problem& p, const Split& s, int32_t out_dtype, cudaStream_t st);
+cudaError_t launch_combine_flat(int n_splits, int rows, int D, const float* part_o, const float* part_lse,
+                                int32_t out_dtype, void* o, int64_t o_row_stride, float* lse,
+                                int masked_zero, cudaStream_t st);
+
+}  // namespace attn

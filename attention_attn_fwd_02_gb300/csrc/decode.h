@@ -1,0 +1,10 @@
+// decode.h -- bandwidth-bound split-range decode pass.
+#pragma once
+#include "common.cuh"
+
+namespace attn {
+// Launches the specialised decode split pass when the problem fits it
+// (f16/bf16, head_dim 64 or 128, contiguous 16-byte-aligned cache rows).
+// Sets *used = 1 when it launched; returns an ATTN_* status.
+int decode_fast_try(const Problem& p, const Split& s, cudaStream_t st, int* used);
+}  // namespace attn

@@ -1,0 +1,10 @@
+// prefill_tc.h -- tensor-core (tcgen05 + TMEM + TMA) prefill path.
+#pragma once
+#include "common.cuh"
+
+namespace attn {
+// Launches the tensor-core kernel when the problem fits it (f16/bf16, a
+// head_dim it is built for, a layout TMA can describe).  Sets *used = 1 when
+// it launched; returns an ATTN_* status.
+int prefill_tc_try(const Problem& p, cudaStream_t st, int* used);
+}  // namespace attn

@@ -1,0 +1,305 @@
+// simt.cu -- CUDA-core kernels: the exact float32 forward (also the generic
+// fallback for half/bfloat16 layouts the tensor-core path cannot take), the
+// generic split-range decode pass, and the partial-result combine.
+//
+// The forward follows the online normaliser of "Attention" (recursiveai.org
+// OneGPU docs), opening paragraph, and the per-block steps of
+// "attention_forward -- Causal Multi-Head Attention with Online Softmax"
+// (llm.istanbul), section "Online Softmax Algoritmasi": per tile of keys take
+// the tile maximum, rescale the running sum and accumulator by
+// exp(m_old - m_new), add the tile's exp(s - m_new) terms.  Each tile's
+// products go into a fresh accumulator that is added after the one rescale
+// ("Attention", section "Accuracy at long key lengths": blockwise summation).
+//
+// Layout of the work: a CTA of 128 threads owns 128/TPR query rows of one
+// (batch, kv head) pair; TPR threads (4 to 32) share a row, each holding up to
+// 8 of its head_dim elements (element d lives in lane d % TPR, slot d / TPR).  Rows are
+// ordered (query, head-in-group), so the heads that share a key/value head
+// read each staged key tile once.  Dot products are reduced over the TPR lanes
+// with an xor butterfly, which gives every lane the same bits; every sum has a
+// fixed order, so results are deterministic.
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kSlots = 8;    // head_dim elements per thread
+constexpr int kTile = 32;    // keys per staged tile
+
+template <typename T, int TPR>
+__global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp, int64_t row_blocks) {
+  constexpr int RPC = kThreads / TPR;  // rows per CTA
+  extern __shared__ float smem[];
+  float* Ks = smem;
+  float* Vs = smem + kTile * p.D;
+  __shared__ int s_lo, s_hi;
+
+  // Linear block index -> (split, batch*kv_head, row block).
+  int64_t blk = blockIdx.x;
+  const int rb = (int)(blk % row_blocks);
+  blk /= row_blocks;
+  const int bg = (int)(blk % ((int64_t)p.B * p.G));
+  const int split = (int)(blk / ((int64_t)p.B * p.G));
+  const int b = bg / p.G, g = bg % p.G;
+  const int D = p.D;
+
+  const int64_t k0 = (int64_t)split * sp.split_len;
+  const int64_t k1 = min((int64_t)p.Sk, k0 + (int64_t)sp.split_len);
+  const int rl = threadIdx.x / TPR, lr = threadIdx.x % TPR;
+  const int64_t r = (int64_t)rb * RPC + rl;
+  const bool valid = r < (int64_t)p.Sq * p.qpg;
+  const int i = valid ? (int)(r / p.qpg) : 0;
+  const int h = g * p.qpg + (valid ? (int)(r % p.qpg) : 0);
+
+  int64_t lo = 0, hi = 0;
+  if (valid) {
+    row_range(p, b, i, lo, hi);
+    lo = max(lo, k0);
+    hi = min(hi, k1);
+    if (hi < lo) hi = lo;
+  }
+  if (threadIdx.x == 0) {
+    s_lo = INT_MAX;
+    s_hi = INT_MIN;
+  }
+  __syncthreads();
+  if (valid && lr == 0 && hi > lo) {
+    atomicMin(&s_lo, (int)lo);
+    atomicMax(&s_hi, (int)hi);
+  }
+  __syncthreads();
+  const int u_lo = s_lo, u_hi = s_hi;  // union of the CTA's row ranges (empty: u_lo > u_hi)
+
+  const T* Q = static_cast<const T*>(p.Q);
+  const T* K = static_cast<const T*>(p.K);
+  const T* V = static_cast<const T*>(p.V);
+  const int64_t qb = p.q.off + (int64_t)b * p.q.bs + (int64_t)h * p.q.hs + (int64_t)i * p.q.rs;
+  const int64_t kb = p.k.off + (int64_t)b * p.k.bs + (int64_t)g * p.k.hs;
+  const int64_t vb = p.v.off + (int64_t)b * p.v.bs + (int64_t)g * p.v.hs;
+  const int64_t mrow = p.M ? p.m.off + (int64_t)b * p.m.bs + (int64_t)h * p.m.hs + (int64_t)i * p.m.rs : 0;
+
+  float qr[kSlots], acc[kSlots];
+#pragma unroll
+  for (int s = 0; s < kSlots; ++s) {
+    const int d = lr + TPR * s;
+    qr[s] = (valid && d < D) ? to_f32(Q[qb + d]) : 0.f;
+    acc[s] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+
+  for (int t0 = (u_lo / kTile) * kTile; t0 < u_hi; t0 += kTile) {
+    __syncthreads();
+    // Stage the tile; keys outside the CTA's union are zero (never read from memory).
+    for (int e = threadIdx.x; e < kTile * D; e += kThreads) {
+      const int j = e / D, d = e - j * D;
+      const int kk = t0 + j;
+      float kv = 0.f, vv = 0.f;
+      if (kk >= u_lo && kk < u_hi) {
+        kv = to_f32(K[kb + (int64_t)kk * p.k.rs + d]);
+        vv = to_f32(V[vb + (int64_t)kk * p.v.rs + d]);
+      }
+      Ks[e] = kv;
+      Vs[e] = vv;
+    }
+    __syncthreads();
+
+    float sc[kTile];
+    float mt = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kTile; ++j) {
+      float part = 0.f;
+#pragma unroll
+      for (int s = 0; s < kSlots; ++s) {
+        const int d = lr + TPR * s;
+        if (TPR * s < D && d < D) part = fmaf(qr[s], Ks[j * D + d], part);
+      }
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      const int kk = t0 + j;
+      const bool vis = valid && kk >= lo && kk < hi;
+      float x = p.scale * part;
+      if (vis && p.M) x += p.M[mrow + kk];
+      sc[j] = vis ? x : -INFINITY;
+      mt = fmaxf(mt, sc[j]);
+    }
+    const float m_new = fmaxf(m, mt);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no exp(-inf - -inf)
+    const float corr = expf(m - m_use);
+    float lt = 0.f;
+#pragma unroll
+    for (int j = 0; j < kTile; ++j) {
+      sc[j] = expf(sc[j] - m_use);
+      lt += sc[j];
+    }
+    l = fmaf(l, corr, lt);
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+      const int d = lr + TPR * s;
+      if (TPR * s < D && d < D) {
+        float t = 0.f;
+#pragma unroll
+        for (int j = 0; j < kTile; ++j) t = fmaf(sc[j], Vs[j * D + d], t);
+        acc[s] = fmaf(acc[s], corr, t);
+      }
+    }
+    m = m_new;
+  }
+
+  if (!valid) return;
+  const bool hidden = (l == 0.f);  // no key with non-zero weight; NaN l is a NaN row
+  if (sp.n_splits == 1) {
+    T* O = static_cast<T*>(p.O);
+    const int64_t ob = p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs + (int64_t)i * p.o.rs;
+    const float fill = p.masked_zero ? 0.f : NAN;
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+      const int d = lr + TPR * s;
+      if (TPR * s < D && d < D) O[ob + d] = from_f32<T>(hidden ? fill : acc[s] / l);
+    }
+    if (p.lse && lr == 0)
+      p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + i] = hidden ? -INFINITY : m + logf(l);
+  } else {
+    const int64_t row = ((int64_t)b * p.H + h) * p.Sq + i;
+    float* po = sp.part_o + (row * sp.n_splits + split) * D;
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+      const int d = lr + TPR * s;
+      if (TPR * s < D && d < D) po[d] = hidden ? 0.f : acc[s] / l;
+    }
+    if (lr == 0) sp.part_lse[row * sp.n_splits + split] = hidden ? -INFINITY : m + logf(l);
+  }
+}
+
+// One warp per row: merge the row's range partials in range order.
+template <typename T>
+__global__ void __launch_bounds__(128) combine_kernel(int n_splits, int64_t rows, int D, const float* part_o,
+                                                      const float* part_lse, T* O, Layout ol, int H, int Sq,
+                                                      float* lse, int64_t lse_bs, int64_t lse_hs,
+                                                      int64_t lse_rs, int masked_zero) {
+  const int64_t row = (int64_t)blockIdx.x * 4 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  const float* pl = part_lse + row * n_splits;
+  float M = -INFINITY;
+  bool bad = false;
+  for (int r = 0; r < n_splits; ++r) {
+    const float x = pl[r];
+    if (isnan(x) || x == INFINITY) bad = true;
+    else M = fmaxf(M, x);
+  }
+  const int i = (int)(row % Sq);
+  const int h = (int)((row / Sq) % H);
+  const int64_t b = row / ((int64_t)Sq * H);
+  const int64_t ob = ol.off + b * ol.bs + (int64_t)h * ol.hs + (int64_t)i * ol.rs;
+  float acc[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) acc[s] = 0.f;
+  float ws = 0.f;
+  if (!bad && M != -INFINITY) {
+    for (int r = 0; r < n_splits; ++r) {
+      const float x = pl[r];
+      if (x == -INFINITY) continue;
+      const float w = expf(x - M);
+      ws += w;
+      const float* src = part_o + (row * n_splits + r) * D;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int d = lane + 32 * s;
+        if (d < D) acc[s] = fmaf(w, src[d], acc[s]);
+      }
+    }
+  }
+  float val_fill = NAN;
+  if (!bad && M == -INFINITY) val_fill = masked_zero ? 0.f : NAN;
+  const bool normal = !bad && M != -INFINITY;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int d = lane + 32 * s;
+    if (d < D) O[ob + d] = from_f32<T>(normal ? acc[s] / ws : val_fill);
+  }
+  if (lse && lane == 0)
+    lse[b * lse_bs + (int64_t)h * lse_hs + (int64_t)i * lse_rs] =
+        bad ? NAN : (M == -INFINITY ? -INFINITY : M + logf(ws));
+}
+
+template <typename T, int TPR>
+cudaError_t launch_simt_t(const Problem& p, const Split& s, cudaStream_t st) {
+  constexpr int RPC = kThreads / TPR;
+  const int64_t rows = (int64_t)p.Sq * p.qpg;
+  const int64_t row_blocks = (rows + RPC - 1) / RPC;
+  const int64_t blocks = row_blocks * p.B * p.G * s.n_splits;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
+  const size_t smem = (size_t)2 * kTile * p.D * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(simt_attn_kernel<T, TPR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  simt_attn_kernel<T, TPR><<<(unsigned)blocks, kThreads, smem, st>>>(p, s, row_blocks);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_simt_d(const Problem& p, const Split& s, cudaStream_t st) {
+  if (p.D <= 32) return launch_simt_t<T, 4>(p, s, st);
+  if (p.D <= 64) return launch_simt_t<T, 8>(p, s, st);
+  if (p.D <= 128) return launch_simt_t<T, 16>(p, s, st);
+  return launch_simt_t<T, 32>(p, s, st);
+}
+
+template <typename T>
+cudaError_t launch_combine_t(int n_splits, int64_t rows, int D, const float* po, const float* pl, void* o,
+                             Layout ol, int H, int Sq, float* lse, int64_t lbs, int64_t lhs, int64_t lrs,
+                             int masked_zero, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const int64_t blocks = (rows + 3) / 4;
+  if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
+  combine_kernel<T><<<(unsigned)blocks, 128, 0, st>>>(n_splits, rows, D, po, pl, static_cast<T*>(o), ol, H, Sq,
+                                                      lse, lbs, lhs, lrs, masked_zero);
+  return cudaGetLastError();
+}
+
+cudaError_t combine_dispatch(int32_t dt, int n_splits, int64_t rows, int D, const float* po, const float* pl,
+                             void* o, Layout ol, int H, int Sq, float* lse, int64_t lbs, int64_t lhs,
+                             int64_t lrs, int masked_zero, cudaStream_t st) {
+  switch (dt) {
+    case ATTN_F32:
+      return launch_combine_t<float>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs, masked_zero, st);
+    case ATTN_F16:
+      return launch_combine_t<__half>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs, masked_zero, st);
+    default:
+      return launch_combine_t<__nv_bfloat16>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs,
+                                             masked_zero, st);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_simt(const Problem& p, const Split& s, cudaStream_t st) {
+  switch (p.dtype) {
+    case ATTN_F32: return launch_simt_d<float>(p, s, st);
+    case ATTN_F16: return launch_simt_d<__half>(p, s, st);
+    default: return launch_simt_d<__nv_bfloat16>(p, s, st);
+  }
+}
+
+cudaError_t launch_combine(const Problem& p, const Split& s, int32_t out_dtype, cudaStream_t st) {
+  const int64_t rows = (int64_t)p.B * p.H * p.Sq;
+  return combine_dispatch(out_dtype, s.n_splits, rows, p.D, s.part_o, s.part_lse, p.O, p.o, p.H, p.Sq, p.lse,
+                          p.lse_bs, p.lse_hs, 1, p.masked_zero, st);
+}
+
+cudaError_t launch_combine_flat(int n_splits, int rows, int D, const float* part_o, const float* part_lse,
+                                int32_t out_dtype, void* o, int64_t o_row_stride, float* lse, int masked_zero,
+                                cudaStream_t st) {
+  Layout ol{0, 0, 0, o_row_stride};
+  return combine_dispatch(out_dtype, n_splits, rows, D, part_o, part_lse, o, ol, 1, rows, lse, 0, 0, 1,
+                          masked_zero, st);
+}
+
+}  // namespace attn

@@ -1,0 +1,174 @@
+/*
+ * attn.h -- C ABI of libattn.so: fused softmax attention forward on one GB300.
+ *
+ * Every entry point computes, for each batch entry b, query head h and query
+ * row i,
+ *
+ *     O[b,h,i,:] = softmax_k( scale * Q[b,h,i,:] . K[b,g,k,:] + mask[b,h,i,k] ) V[b,g,k,:]
+ *     LSE[b,h,i] = log sum_k exp( scale * Q . K + mask )          (natural log)
+ *
+ * with g = h / (heads / kv_heads), the sum running over the keys visible to the
+ * row.  Sources: "Attention" (recursiveai.org OneGPU docs), opening paragraph
+ * (the formula and the online normaliser), section "What it covers" (element
+ * types, layouts, lengths, heads, head dimension, masks) and section "Special
+ * values"; "attention_forward -- Causal Multi-Head Attention with Online
+ * Softmax" (llm.istanbul), sections "GQA", "2) Phase 0" (segment starts) and
+ * "Online Softmax Algoritmasi" (LSE = m + log l); "com.microsoft.GroupQueryAttention"
+ * (webgpu-kernels README), section "Inputs" (BNSH key/value caches, per-sample
+ * key lengths, additive attention bias with broadcast leading dimensions).
+ *
+ * Key visibility.  Key k (0 <= k < k_len) is visible to row (b, i) iff
+ *   - k < clamp(k_lens[b], 0, k_len)          when k_lens is given, and
+ *   - k <= i + causal_offset                  when causal != 0, and
+ *   - k >= clamp(seg[b, i], 0, k_len)         when seg is given,
+ * and its weight is zero when mask[b,h,i,k] = -inf.  A visible key whose score
+ * is NaN or +inf makes the whole row NaN (O and LSE).  A row with no key of
+ * non-zero weight (k_len = 0 included) gives NaN in every O element, or 0
+ * under ATTN_MASKED_ROWS_ZERO, and LSE = -inf.  Out-of-range k_lens and seg
+ * values are clamped to [0, k_len] (a convention of this library).
+ *
+ * Memory.  Every data pointer is a DEVICE pointer owned by the caller.  The
+ * library allocates no device memory: scratch space is the caller's
+ * `workspace` (size from the *_workspace_size queries).  K/V values of keys
+ * that are hidden from every query row of a 128-row query tile are never read
+ * into the result; V values of a key that some row of the tile sees must be
+ * finite, or rows of that tile that hide the key may become NaN (tensor-core
+ * products multiply them by zero).
+ *
+ * Execution.  Calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream): they validate on the host, enqueue kernels and
+ * return.  No call synchronises the host except attn_device_status.  No C++
+ * exception crosses the ABI.  Results are deterministic: every sum has a
+ * fixed order and no float atomics are used, so two runs give identical bits.
+ * Calls on one stream are serialised by the stream; concurrent calls on
+ * different streams must not share output or workspace buffers.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* attn_stream;
+
+/* Element type of Q, K, V and O.  The mask and LSE are always float32. */
+enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 };
+
+/* What a row with no visible key returns ("Attention", section "Special values"). */
+enum { ATTN_MASKED_ROWS_NAN = 0, ATTN_MASKED_ROWS_ZERO = 1 };
+
+/* Status codes. */
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* null required pointer, negative size, heads % kv_heads != 0,
+                                  head_dim outside [1, 256], odd head_dim for f16/bf16, bad layout */
+  ATTN_ERR_UNSUPPORTED = 2,    /* a valid combination this build does not implement */
+  ATTN_ERR_ALIGNMENT = 3,      /* a pointer not aligned to its element size */
+  ATTN_ERR_WORKSPACE = 4,      /* workspace missing or smaller than the size query says */
+  ATTN_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up a bounded wait (see attn_device_status) */
+};
+
+/* ATTN_OFFSET_DEFAULT as causal_offset selects k_len - q_len ("Attention",
+ * section "What it covers": the cached-decoder default). */
+#define ATTN_OFFSET_DEFAULT INT64_MIN
+
+/* A strided 4-D view [batch][head][row][element]: element (b, h, r, e) is at
+ * base[offset + b*batch_stride + h*head_stride + r*row_stride + e].  Strides
+ * are in elements; the elements of a row are contiguous.  Position-first
+ * [B, S, H, D] is {0, S*H*D, D, H*D}; head-first [B, H, S, D] is
+ * {0, H*S*D, S*D, D}; a slice of a packed QKV projection sets offset. */
+typedef struct {
+  int64_t offset, batch_stride, head_stride, row_stride;
+} attn_layout;
+
+/* The problem ("Attention", section "What it covers"; P(batch, heads, qLen,
+ * kLen, headDim) of that page's example, plus kv_heads for grouped heads). */
+typedef struct {
+  int32_t batch, heads, kv_heads;  /* heads % kv_heads == 0 */
+  int32_t q_len, k_len;            /* k_len is the cache capacity for attn_decode */
+  int32_t head_dim;                /* 1..256; even for f16/bf16 */
+  int32_t dtype;                   /* ATTN_F32 / ATTN_F16 / ATTN_BF16 */
+  float scale;                     /* 0 selects the float nearest 1/sqrt(head_dim) */
+  int32_t causal;                  /* 0 or 1 */
+  int64_t causal_offset;           /* used iff causal; ATTN_OFFSET_DEFAULT = k_len - q_len */
+  int32_t masked_rows;             /* ATTN_MASKED_ROWS_NAN / ATTN_MASKED_ROWS_ZERO */
+  attn_layout q, k, v, o;          /* Q, O over heads; K, V over kv_heads */
+  attn_layout mask;                /* float32 mask strides over (batch, head, row); 0 broadcasts;
+                                      keys contiguous.  Ignored when mask == NULL. */
+  int64_t seg_batch_stride;        /* seg is int32 [batch][q_len] with this batch stride (0 shares one row set) */
+  int64_t lse_batch_stride;        /* LSE float32 element (b, h, i) at lse[b*lse_batch_stride + */
+  int64_t lse_head_stride;         /*   h*lse_head_stride + i] */
+} attn_problem;
+
+/* Bytes of device workspace attn_fwd needs for this problem (0 when none).
+ * Returns 0 also for an invalid problem; attn_fwd then reports the error. */
+ATTN_API size_t attn_fwd_workspace_size(const attn_problem* p);
+
+/* Prefill / full forward.  q, k, v, o: device pointers in p->dtype laid out
+ * by p->q, p->k, p->v, p->o.  mask (nullable): float32, strides p->mask.
+ * seg (nullable): int32 segment starts.  k_lens (nullable): int32 [batch]
+ * key counts.  lse (nullable): float32 output.  workspace: device scratch of
+ * at least attn_fwd_workspace_size(p) bytes (NULL when that is 0).
+ * batch == 0 or q_len == 0 is a no-op returning ATTN_OK. */
+ATTN_API int attn_fwd(const attn_problem* p, const void* q, const void* k, const void* v, void* o,
+             const float* mask, const int32_t* seg, const int32_t* k_lens, float* lse,
+             void* workspace, size_t workspace_bytes, attn_stream stream);
+
+/* Bytes of device workspace attn_decode needs (per-range partial results). */
+ATTN_API size_t attn_decode_workspace_size(const attn_problem* p);
+
+/* Single-query decode against a key/value cache: q_len must be 1.  The keys
+ * are cut into ranges whose size depends only on the shape (k_len, batch,
+ * kv_heads); each range writes a partial (LSE, O) into the workspace and a
+ * second kernel merges them in range order (the split-K decode of
+ * "com.microsoft.GroupQueryAttention", section "Implementation variants",
+ * and the key-range split of "Attention", section "Accuracy at long key
+ * lengths").  k_cache/v_cache are laid out by p->k/p->v (BNSH cache:
+ * {0, kv_heads*cap*D, cap*D, D}); k_lens (nullable) holds each sample's
+ * number of valid cache rows (an ONNX seqlens_k value plus one).  mask, seg and
+ * lse are as for attn_fwd and may be NULL. */
+ATTN_API int attn_decode(const attn_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                void* o, const float* mask, const int32_t* seg, const int32_t* k_lens, float* lse,
+                void* workspace, size_t workspace_bytes, attn_stream stream);
+
+/* Merge per-range partial results of `rows` rows ("Attention", section
+ * "Accuracy at long key lengths": partials merged in range order).
+ * part_o: float32 [rows][n_splits][head_dim], each already divided by its own
+ * sum; part_lse: float32 [rows][n_splits] (-inf marks an empty range).  The
+ * row result is O = sum_r exp(lse_r) O_r / sum_r exp(lse_r) and
+ * LSE = log sum_r exp(lse_r), written to o (out_dtype, row r at
+ * o + r*o_row_stride elements) and lse (nullable, float32 [rows]).  A NaN or
+ * +inf lse_r makes the row NaN; all ranges empty gives a masked row. */
+ATTN_API int attn_combine(int32_t n_splits, int32_t rows, int32_t head_dim, const float* part_o,
+                 const float* part_lse, int32_t out_dtype, void* o, int64_t o_row_stride, float* lse,
+                 int32_t masked_rows, attn_stream stream);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT when a
+ * kernel abandoned a bounded wait since the last call (its outputs are then
+ * undefined).  Returns ATTN_ERR_CUDA if synchronising fails. */
+ATTN_API int attn_device_status(attn_stream stream);
+
+/* Static description of a status code. */
+ATTN_API const char* attn_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

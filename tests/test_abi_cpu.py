@@ -1,0 +1,133 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/attn.h declares, its struct layout matches the binding's, and
+host-side argument checks return their status codes before touching CUDA."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from attention_attn_fwd_02_gb300 import attn, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return attn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(declared_functions()) == sorted(attn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", attn.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    syms = set(re.findall(r"\bT\s+(attn_\w+)", out))
+    for name in declared_functions():
+        assert name in syms, name
+        assert hasattr(L, name)
+
+
+def test_struct_layout_matches_c(tmp_path):
+    src = tmp_path / "sz.c"
+    src.write_text(f'#include "{HEADER}"\n#include <stdio.h>\n#include <stddef.h>\n'
+                   'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(attn_problem),'
+                   ' offsetof(attn_problem, causal_offset), offsetof(attn_problem, q),'
+                   ' offsetof(attn_problem, mask), offsetof(attn_problem, seg_batch_stride),'
+                   ' offsetof(attn_problem, lse_head_stride)); return 0;}\n')
+    exe = tmp_path / "sz"
+    subprocess.run(["gcc", str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P = attn.attn_problem
+    want = [ctypes.sizeof(P), P.causal_offset.offset, P.q.offset, P.mask.offset, P.seg_batch_stride.offset,
+            P.lse_head_stride.offset]
+    assert got == want
+
+
+def base_problem(**kw):
+    d = dict(batch=2, heads=4, kv_heads=2, q_len=8, k_len=8, head_dim=64, dtype="bf16",
+             q_layout=(0, 8 * 4 * 64, 64, 4 * 64), k_layout=(0, 8 * 2 * 64, 64, 2 * 64),
+             v_layout=(0, 8 * 2 * 64, 64, 2 * 64), o_layout=(0, 8 * 4 * 64, 64, 4 * 64))
+    d.update(kw)
+    return attn.make_problem(d)
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails on the host first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kv_heads=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(head_dim=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(head_dim=257), attn.ATTN_ERR_INVALID_ARG),
+    (dict(head_dim=63), attn.ATTN_ERR_INVALID_ARG),          # half types need an even head_dim
+    (dict(dtype=7), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q_len=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(heads=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q_layout=(0, -1, 64, 256)), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(masked_rows=5), attn.ATTN_ERR_INVALID_ARG),
+])
+def test_fwd_rejects_invalid_problems(L, kw, code):
+    p = base_problem(**kw)
+    if "causal" in kw:
+        p.causal = kw["causal"]
+    if "masked_rows" in kw:
+        p.masked_rows = kw["masked_rows"]
+    assert attn.attn_fwd(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None, 0, None) == code
+
+
+def test_fwd_null_and_misaligned_pointers(L):
+    p = base_problem()
+    assert attn.attn_fwd(p, None, FAKE, FAKE, FAKE, None, None, None, None, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd(p, FAKE, FAKE, FAKE, None, None, None, None, None, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd(p, FAKE + 1, FAKE, FAKE, FAKE, None, None, None, None, None, 0, None) == attn.ATTN_ERR_ALIGNMENT
+    assert attn.attn_fwd(p, FAKE, FAKE, FAKE, FAKE, FAKE + 2, None, None, None, None, 0, None) == attn.ATTN_ERR_ALIGNMENT
+
+
+def test_empty_problems_are_noops(L):
+    assert attn.attn_fwd(base_problem(batch=0), None, None, None, None, None, None, None, None, None, 0, None) == 0
+    assert attn.attn_fwd(base_problem(q_len=0), None, None, None, None, None, None, None, None, None, 0, None) == 0
+
+
+def test_decode_checks(L):
+    p = base_problem(q_len=2)
+    assert attn.attn_decode_workspace_size(p) == 0
+    assert attn.attn_decode(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, 1 << 20,
+                            None) == attn.ATTN_ERR_INVALID_ARG
+    p = base_problem(q_len=1, k_len=8192)
+    need = attn.attn_decode_workspace_size(p)
+    assert need > 0 and need % 256 == 0
+    assert attn.attn_decode(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None, 0,
+                            None) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_decode(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE, need - 1,
+                            None) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_decode(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, FAKE + 16, need,
+                            None) == attn.ATTN_ERR_ALIGNMENT
+
+
+def test_combine_checks(L):
+    assert attn.attn_combine(4, 0, 64, None, None, 0, None, 64, None, 0, None) == 0
+    assert attn.attn_combine(4, 3, 0, FAKE, FAKE, 0, FAKE, 64, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_combine(4, 3, 64, FAKE, FAKE, 9, FAKE, 64, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_combine(4, 3, 64, None, FAKE, 0, FAKE, 64, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_combine(4, 3, 64, FAKE, FAKE, 1, FAKE + 1, 64, None, 0, None) == attn.ATTN_ERR_ALIGNMENT
+
+
+def test_status_strings_and_version(L):
+    for code in range(7):
+        assert attn.status_string(code) and attn.status_string(code) != "unknown status"
+    assert attn.status_string(99) == "unknown status"
+    assert attn.attn_version() >= 100

@@ -1,0 +1,218 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Small and medium cases compare every element; the full-size workloads compare
+sampled rows the oracle computes one by one.  Bars: float32 per element
+|d| <= 2e-6 (1 + |O|); f16/bf16 |d| <= 1.5e-2 absolute; LSE |d| <= 1e-3;
+NaN / zero row classes exact; plus the scaled-error bounds of "Attention"
+(recursiveai.org OneGPU docs), section "Tolerances".
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from attention_attn_fwd_02_gb300 import attn, build
+from attention_attn_fwd_02_gb300 import workloads as wl
+from gpu_util import GpuCase, compare, oracle_full, torch_mod
+
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = torch_mod()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    attn.lib()
+
+
+def run_and_compare(case, lse=True, where=None):
+    g = GpuCase(case, lse=lse).run()
+    o, l, _ = g.outputs()
+    g.check_guards()
+    ref_o, ref_l = oracle_full(case)
+    st = compare(o, l, ref_o, ref_l if lse else None, case.problem["dtype"], case.problem["masked_rows"],
+                 where or case.name)
+    assert attn.attn_device_status() == attn.ATTN_OK
+    return st, g
+
+
+# ---- the named workloads (reduced where the full size is sampled below) ---------------------
+
+
+def test_tiny_f32_mha():
+    run_and_compare(wl.tiny_f32_mha())
+
+
+def test_gqa_doc_causal_bf16_full():
+    run_and_compare(wl.gqa_doc_causal_bf16())
+
+
+def test_long_causal_gqa_bf16_reduced():
+    run_and_compare(wl.long_causal_gqa_bf16(batch=2, seq=640, heads=8, kv_heads=2))
+
+
+@pytest.mark.parametrize("cap", [1024, 8192])
+def test_decode_bnsh_bf16_reduced(cap):
+    run_and_compare(wl.decode_bnsh_bf16(batch=4, capacity=cap, heads=32, kv_heads=8, min_len=1), lse=True)
+
+
+@pytest.mark.parametrize("masked_rows", ["nan", "zero"])
+def test_cross_mask_f16_reduced(masked_rows):
+    c = wl.cross_mask_f16(batch=3, q_len=130, k_len=300, heads=2, masked_rows=masked_rows)
+    st, _ = run_and_compare(c)
+    assert st["nan_rows"] == (2 * 130 if masked_rows == "nan" else 0)
+
+
+# ---- edge sweep ---------------------------------------------------------------------------
+
+EDGE = [
+    # dtype, layout, B, H, G, Sq, Sk, D, causal, offset, seg, lens, mask, masked_rows, packed
+    ("f32", "bshd", 1, 1, 1, 1, 1, 1, False, None, False, False, None, "nan", False),
+    ("f32", "bhsd", 2, 3, 1, 33, 65, 31, True, None, False, False, None, "nan", False),
+    ("f32", "bshd", 1, 4, 2, 129, 127, 33, True, 5, True, True, "bhqk", "zero", False),
+    ("f32", "bshd", 2, 2, 2, 7, 0, 16, False, None, False, False, None, "nan", False),
+    ("f32", "bshd", 2, 2, 2, 7, 0, 16, False, None, False, False, None, "zero", False),
+    ("bf16", "bshd", 2, 8, 1, 200, 200, 64, True, 0, True, False, None, "nan", False),
+    ("bf16", "bhsd", 1, 6, 3, 129, 1000, 128, True, None, False, True, "b11k", "nan", False),
+    ("bf16", "bshd", 2, 4, 4, 128, 128, 96, True, -3, False, False, None, "zero", False),
+    ("f16", "bshd", 1, 2, 2, 65, 257, 256, False, None, False, True, "b11k", "nan", False),
+    ("f16", "bhsd", 2, 32, 1, 17, 300, 2, True, 100, True, True, None, "nan", False),
+    ("bf16", "bshd", 2, 4, 2, 150, 150, 64, True, None, False, False, None, "nan", True),
+    ("f16", "bshd", 1, 2, 1, 127, 127, 200, False, None, False, False, "11qk", "zero", True),
+    ("bf16", "bhsd", 3, 2, 2, 1, 513, 128, False, None, False, True, None, "nan", False),
+    ("f32", "bhsd", 1, 2, 2, 300, 300, 256, True, None, False, False, None, "nan", False),
+]
+
+
+def make_edge(i, e):
+    dtype, layout, B, H, G, Sq, Sk, D, causal, off, use_seg, use_lens, mk, mr, packed = e
+    r = np.random.default_rng(1000 + i)
+    seg = np.sort(r.integers(0, max(1, Sk), size=(B, Sq)), axis=1).astype(np.int32) if use_seg else None
+    k_lens = None
+    if use_lens:
+        k_lens = r.integers(0, Sk + 1, size=B).astype(np.int32)
+        k_lens[0] = Sk if B > 1 else k_lens[0]
+    mask = None
+    if mk is not None:
+        shape = {"bhqk": (B, H, Sq, Sk), "b11k": (B, 1, 1, Sk), "11qk": (1, 1, Sq, Sk)}[mk]
+        mask = r.standard_normal(shape).astype(np.float32)
+        mask[r.random(shape) < 0.2] = -np.inf
+    return wl.make_case(name=f"edge{i}", seed=2000 + i, dtype=dtype, layout=layout, batch=B, heads=H, kv_heads=G,
+                        q_len=Sq, k_len=Sk, head_dim=D, causal=causal, causal_offset=off, seg=seg,
+                        k_lens=k_lens, mask=mask, mask_kind=mk or "b11k", masked_rows=mr, packed=packed)
+
+
+@pytest.mark.parametrize("i", range(len(EDGE)))
+def test_edge_sweep(i):
+    run_and_compare(make_edge(i, EDGE[i]))
+
+
+def test_nan_and_inf_scores_make_nan_rows():
+    B, H, Sq, Sk, D = 1, 2, 40, 70, 64
+    mask = np.zeros((B, 1, 1, Sk), dtype=np.float32)
+    mask[0, 0, 0, 5] = np.nan
+    c = wl.make_case(name="nan_score", seed=31, dtype="bf16", batch=B, heads=H, q_len=Sq, k_len=Sk, head_dim=D,
+                     causal=True, causal_offset=0, mask=mask)
+    st, _ = run_and_compare(c)
+    assert st["nan_rows"] == H * (Sq - 5)
+    mask[0, 0, 0, 5] = np.inf
+    mask[0, 0, 0, :5] = -np.inf
+    c = wl.make_case(name="inf_score", seed=31, dtype="bf16", batch=B, heads=H, q_len=Sq, k_len=Sk, head_dim=D,
+                     causal=True, causal_offset=0, mask=mask, masked_rows="zero")
+    run_and_compare(c)
+
+
+# ---- structural properties ------------------------------------------------------------------
+
+
+def test_rerun_is_bit_identical():
+    c = wl.long_causal_gqa_bf16(batch=1, seq=700, heads=4, kv_heads=2)
+    g = GpuCase(c).run()
+    _, l1, o1 = g.outputs()
+    g.run()
+    _, l2, o2 = g.outputs()
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2, equal_nan=True)
+
+
+def test_single_visible_key_is_exact():
+    B, H, S, D = 2, 4, 260, 128
+    seg = np.tile(np.arange(S, dtype=np.int32), (B, 1))
+    c = wl.make_case(name="single_key", seed=41, dtype="bf16", layout="bhsd", batch=B, heads=H, q_len=S,
+                     head_dim=D, causal=True, causal_offset=0, seg=seg)
+    g = GpuCase(c).run()
+    _, _, raw = g.outputs()
+    v = c.v.reshape(B, H, S, D)
+    assert np.array_equal(raw, v)
+
+
+def test_gqa_equals_repeated_heads():
+    B, H, G, S, D = 1, 8, 2, 300, 64
+    c = wl.make_case(name="gqa", seed=43, dtype="bf16", layout="bhsd", batch=B, heads=H, kv_heads=G, q_len=S,
+                     head_dim=D, causal=True)
+    c2 = wl.make_case(name="mha", seed=43, dtype="bf16", layout="bhsd", batch=B, heads=H, kv_heads=G, q_len=S,
+                      head_dim=D, causal=True)
+    c2.k = np.repeat(c.k.reshape(B, G, S, D), H // G, axis=1).copy()
+    c2.v = np.repeat(c.v.reshape(B, G, S, D), H // G, axis=1).copy()
+    c2.problem = dict(c.problem, kv_heads=H, k_layout=wl.layout_of("bhsd", B, H, S, D)[1],
+                      v_layout=wl.layout_of("bhsd", B, H, S, D)[1])
+    _, l1, o1 = GpuCase(c).run().outputs()
+    _, l2, o2 = GpuCase(c2).run().outputs()
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_hidden_keys_filled_with_nan_are_not_read():
+    c = wl.long_causal_gqa_bf16(batch=2, seq=384, heads=4, kv_heads=1)
+    assert c.k_lens.min() < 384
+    st, _ = run_and_compare(c)
+    assert st["nan_rows"] == 0
+
+
+def test_combine_matches_oracle():
+    torch = torch_mod()
+    r = np.random.default_rng(51)
+    rows, n, D = 37, 5, 72
+    po = r.standard_normal((rows, n, D)).astype(np.float32)
+    pl = (r.standard_normal((rows, n)) * 3).astype(np.float32)
+    pl[r.random((rows, n)) < 0.3] = -np.inf
+    pl[3] = -np.inf
+    pl[4, 2] = np.nan
+    pl[5, 1] = np.inf
+    for mr in ("nan", "zero"):
+        ref_o, ref_l = oracle.combine(po, pl, masked_rows=mr)
+        for dt, tol in ((torch.float32, 1e-6), (torch.bfloat16, 1.5e-2)):
+            o, l = attn.combine(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda(), out_dtype=dt,
+                                masked_rows=mr, return_lse=True)
+            o = o.float().cpu().numpy().astype(np.float64)
+            l = l.cpu().numpy().astype(np.float64)
+            assert np.array_equal(np.isnan(o), np.isnan(ref_o))
+            f = np.isfinite(ref_o)
+            assert np.all(np.abs(o[f] - ref_o[f]) <= tol * (1 + np.abs(ref_o[f])))
+            assert np.array_equal(np.isnan(l), np.isnan(ref_l)) and np.array_equal(np.isneginf(l), np.isneginf(ref_l))
+            fl = np.isfinite(ref_l)
+            assert np.allclose(l[fl], ref_l[fl], atol=1e-5)
+
+
+def test_key_range_split_then_combine_equals_one_call():
+    """Two attn_fwd calls on disjoint key ranges merged by attn_combine equal one call."""
+    torch = torch_mod()
+    B, H, Sq, Sk, D = 1, 4, 100, 600, 128
+    c = wl.make_case(name="split", seed=61, dtype="bf16", layout="bhsd", batch=B, heads=H, q_len=Sq, k_len=Sk,
+                     head_dim=D)
+    full_o, full_l = oracle_full(c)
+    kk = torch.from_numpy(c.k.view(np.int16)).cuda().view(torch.bfloat16).reshape(B, H, Sk, D)
+    vv = torch.from_numpy(c.v.view(np.int16)).cuda().view(torch.bfloat16).reshape(B, H, Sk, D)
+    qq = torch.from_numpy(c.q.view(np.int16)).cuda().view(torch.bfloat16).reshape(B, H, Sq, D)
+    parts = []
+    for a, b in ((0, 250), (250, 600)):
+        o, l = attn.fwd(qq, kk[:, :, a:b], vv[:, :, a:b], layout="bhsd", scale=float(np.float32(1 / np.sqrt(D))),
+                        return_lse=True)
+        parts.append((o.float(), l))
+    po = torch.stack([p[0] for p in parts], dim=3).reshape(B * H * Sq, 2, D).contiguous()
+    pl = torch.stack([p[1] for p in parts], dim=3).reshape(B * H * Sq, 2).contiguous()
+    o, l = attn.combine(po, pl, out_dtype=torch.bfloat16, return_lse=True)
+    o = o.float().cpu().numpy().reshape(B, H, Sq, D)
+    assert np.max(np.abs(o - full_o)) <= 2e-2
+    assert np.max(np.abs(l.cpu().numpy().reshape(B, H, Sq) - full_l)) <= 1e-3
