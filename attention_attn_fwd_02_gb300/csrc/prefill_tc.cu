@@ -1,11 +1,677 @@
-// prefill_tc.cu -- tensor-core prefill (placeholder until the kernel lands).
+// prefill_tc.cu -- tensor-core prefill for sm_103a: TMA-staged Q/K/V tiles,
+// S = Q K^T and O += P V as tcgen05 MMAs with TMEM accumulators, online
+// softmax in warp-specialised registers.
+//
+// What it computes: O = softmax(scale * Q K^T + mask) V with the online
+// normaliser of "Attention" (recursiveai.org OneGPU docs), opening paragraph,
+// and the per-tile steps of "attention_forward -- Causal Multi-Head Attention
+// with Online Softmax" (llm.istanbul), section "Online Softmax Algoritmasi".
+// Two refinements from "Attention", section "Apple simdgroup kernel": each
+// row keeps a reference maximum that is raised only when a tile's maximum
+// exceeds it by more than a slack (here 8 in log2 units, so exp2(x - m) <= 256
+// in the probabilities), and the accumulator is rescaled only on a raise; and
+// from section "Matrix hardware": the probabilities are rounded to the element
+// type before the P V product.
+//
+// CTA: 320 threads, two 128-row query tiles (256 rows) of one (batch, head).
+//   warps 0-3  softmax for query tile 0 (thread = one row = one TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp 8     TMA producer (Q once, then K and V tiles through a ring)
+//   warp 9     TMEM owner and MMA issuer (one elected lane issues)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them; the
+// probabilities P overwrite the first BN/2 columns of their S tile as packed
+// 16-bit pairs and feed the second MMA straight from TMEM.
+//
+// The two query tiles ping-pong: while the softmax warps of one tile work on
+// S, the tensor core runs P V and the next Q K^T of the other tile.
+//
+// Every wait is bounded: after ~2 s a waiter raises a CTA abort flag and the
+// library status word (ATTN_ERR_DEVICE_TIMEOUT); every role then leaves its
+// loop, waits (bounded) for its own copies and MMAs in flight, and the TMEM
+// owner frees TMEM before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+#include <type_traits>
+
 #include "prefill_tc.h"
 
 namespace attn {
-int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
-  (void)p;
-  (void)st;
-  *used = 0;
-  return ATTN_OK;
+namespace tc {
+
+constexpr int BM = 128;            // query rows per tile
+constexpr int BN = 128;            // keys per tile
+constexpr int kThreads = 320;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kSlack = 8.0f;     // log2 units
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int lo_u, hi_u;
+};
+
+// ---- PTX wrappers ------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `b` with parity `parity`.
+__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, Bars* sb, int* status) {
+  if (mbar_try(b, parity)) return true;
+  const uint64_t t0 = gtimer();
+  while (!mbar_try(b, parity)) {
+    if (*(volatile int*)&sb->abort) return false;
+    if (gtimer() - t0 > kTimeoutNs) {
+      *(volatile int*)&sb->abort = 1;
+      atomicExch(status, ATTN_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Teardown wait: bounded, does not look at the abort flag.
+__device__ __forceinline__ bool drain_bar(uint64_t* b, uint32_t parity, int* status) {
+  const uint64_t t0 = gtimer();
+  while (!mbar_try(b, parity)) {
+    if (gtimer() - t0 > kTimeoutNs) {
+      atomicExch(status, ATTN_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-uniform bounded wait: every lane waits, and the warp proceeds only if
+// all lanes saw the phase complete, so warp-collective TMEM instructions that
+// follow never run with part of the warp.
+__device__ __forceinline__ bool wait_warp(uint64_t* b, uint32_t parity, Bars* sb, int* status) {
+  const bool ok = wait_bar(b, parity, sb, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
+               : "memory");
+}
+
+#define ATTN_R32(r)                                                                                                 \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),       \
+      "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),        \
+      "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),       \
+      "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define ATTN_W32(r)                                                                                                 \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),    \
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),   \
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),   \
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : ATTN_R32(r)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      ATTN_W32(r)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start,
+// leading and stride byte offsets in 16-byte units, descriptor version 1).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with f32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;                  // 64-column (128-byte) chunks
+  static constexpr int kStages = D <= 64 ? 4 : 2;
+  static constexpr int kQTile = BM * D * 2;               // bytes
+  static constexpr int kKTile = BN * D * 2;
+  static constexpr int kSmem = 2 * kQTile + 2 * kStages * kKTile;
+  static constexpr int kS0 = 0, kS1 = BN, kO0 = 2 * BN, kO1 = 2 * BN + D;
+  static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
+};
+
+template <int D, bool BF16, bool MASK>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem;
+  uint8_t* k_s = q_s + 2 * C::kQTile;
+  uint8_t* v_s = k_s + C::kStages * C::kKTile;
+  __shared__ Bars sb;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // Heaviest query blocks first: block L covers query block n_qblocks-1-L/(H*B).
+  const int HB = p.H * p.B;
+  const int hb = blockIdx.x % HB;
+  const int qb = n_qblocks - 1 - (int)(blockIdx.x / HB);
+  const int h = hb % p.H, b = hb / p.H;
+  const int g = h / p.qpg;
+  const int q0 = qb * 2 * BM;
+
+  // ---- row ranges and their union ----
+  const int t = warp / 4;                       // query tile of a softmax thread
+  const int r = (warp % 4) * 32 + lane;         // row within the tile = TMEM lane
+  const int qrow = q0 + t * BM + r;
+  int lo = 0, hi = 0;
+  if (warp < 8 && qrow < p.Sq) {
+    int64_t lo64, hi64;
+    row_range(p, b, qrow, lo64, hi64);
+    lo = (int)lo64;
+    hi = (int)(hi64 > lo64 ? hi64 : lo64);
+  }
+  if (threadIdx.x == 0) {
+    sb.lo_u = 0x7fffffff;
+    sb.hi_u = -1;
+    sb.abort = 0;
+    mbar_init(&sb.q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&sb.k_full[s], 1);
+      mbar_init(&sb.k_empty[s], 1);
+      mbar_init(&sb.v_full[s], 1);
+      mbar_init(&sb.v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sb.s_full[i], 1);
+      mbar_init(&sb.p_full[i], BM);
+      mbar_init(&sb.o_done[i], 1);
+    }
+    mbar_init(&sb.mma_done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&sb.tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp < 8 && hi > lo) {
+    atomicMin(&sb.lo_u, lo);
+    atomicMax(&sb.hi_u, hi);
+  }
+  __syncthreads();
+  const uint32_t tmem = sb.tmem_base;
+  const int lo_u = sb.lo_u, hi_u = sb.hi_u;
+  const bool any = hi_u > lo_u;
+  const int j0 = any ? lo_u / BN : 0;
+  const int n_tiles = any ? (hi_u + BN - 1) / BN - j0 : 0;
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && n_tiles > 0) {
+      int issued = 0;          // tiles whose K and V copies were both issued
+      int k_only = -1;         // a tile whose K copy was issued but not its V copy
+      mbar_expect_tx(&sb.q_full, 2 * C::kQTile);
+      for (int tt = 0; tt < 2; ++tt)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+        const int krow = (j0 + i) * BN;
+        if (!wait_bar(&sb.k_empty[s], ph ^ 1u, &sb, p.status)) break;
+        mbar_expect_tx(&sb.k_full[s], C::kKTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(k_s + s * C::kKTile + c * BN * 128, &tm_k, &sb.k_full[s], c * 64, krow, g, b);
+        if (!wait_bar(&sb.v_empty[s], ph ^ 1u, &sb, p.status)) {
+          k_only = i;
+          break;
+        }
+        mbar_expect_tx(&sb.v_full[s], C::kKTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(v_s + s * C::kKTile + c * BN * 128, &tm_v, &sb.v_full[s], c * 64, krow, g, b);
+        issued = i + 1;
+      }
+      // Copies still in flight land before the CTA can exit.  A stage's
+      // earlier copies completed before it was refilled, so the last kStages
+      // tiles are the only ones to wait for.
+      drain_bar(&sb.q_full, 0, p.status);
+      for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+        drain_bar(&sb.k_full[s], ph, p.status);
+        drain_bar(&sb.v_full[s], ph, p.status);
+      }
+      if (k_only >= 0) drain_bar(&sb.k_full[k_only % C::kStages], (uint32_t)(k_only / C::kStages) & 1u, p.status);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t kIdQK = idesc_f16(BF16, false, BM, BN);
+    constexpr uint32_t kIdPV = idesc_f16(BF16, true, BM, D);
+    const uint32_t q_addr = su32(q_s), k_addr = su32(k_s), v_addr = su32(v_s);
+    bool ok = n_tiles > 0;
+    if (ok) ok = wait_warp(&sb.q_full, 0, &sb, p.status);
+    auto issue_qk = [&](int tt, int s) {
+      fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t)((kk / 4) * BM * 128 + (kk % 4) * 32);
+        const uint64_t a = sdesc(q_addr + tt * C::kQTile + off, 16, 1024);
+        const uint64_t bd = sdesc(k_addr + s * C::kKTile + (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32), 16, 1024);
+        mma_ss(tmem + (tt ? C::kS1 : C::kS0), a, bd, kIdQK, kk > 0);
+      }
+    };
+    auto issue_pv = [&](int tt, int s, bool first) {
+      fence_after();
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint64_t bd = sdesc(v_addr + s * C::kKTile + kk * 16 * 128, BN * 128, 1024);
+        mma_ts(tmem + (tt ? C::kO1 : C::kO0), tmem + (tt ? C::kS1 : C::kS0) + kk * 8, bd, kIdPV,
+               (!first || kk > 0) ? 1u : 0u);
+      }
+    };
+    // Prologue: S0 and S1 of tile 0.
+    if (ok) ok = wait_warp(&sb.k_full[0], 0, &sb, p.status);
+    if (ok && lane == 0) {
+      issue_qk(0, 0);
+      mma_commit(&sb.s_full[0]);
+      issue_qk(1, 0);
+      mma_commit(&sb.s_full[1]);
+      mma_commit(&sb.k_empty[0]);
+    }
+    __syncwarp();
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int s = i % C::kStages;
+      const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+      const int k0 = (j0 + i) * BN;
+      if (!wait_warp(&sb.v_full[s], ph, &sb, p.status)) break;
+      // Zero the V rows of keys no row of this CTA sees (they may hold anything).
+      if (k0 < lo_u || k0 + BN > hi_u) {
+        for (int u = lane; u < BN * C::kChunks * 8; u += 32) {
+          const int row = u / (C::kChunks * 8);
+          const int rest = u % (C::kChunks * 8);
+          const int kk = k0 + row;
+          if (kk < lo_u || kk >= hi_u) {
+            uint4* dst = reinterpret_cast<uint4*>(v_s + s * C::kKTile + (rest / 8) * BN * 128 + row * 128 +
+                                                  (rest % 8) * 16);
+            *dst = make_uint4(0, 0, 0, 0);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+      const bool more = i + 1 < n_tiles;
+      const int s1 = (i + 1) % C::kStages;
+      const uint32_t ph1 = (uint32_t)((i + 1) / C::kStages) & 1u;
+      // Query tile 0: P0 V, then the next S0.
+      if (!wait_warp(&sb.p_full[0], (uint32_t)i & 1u, &sb, p.status)) break;
+      if (lane == 0) {
+        issue_pv(0, s, i == 0);
+        mma_commit(&sb.o_done[0]);
+      }
+      __syncwarp();
+      if (more) {
+        if (!wait_warp(&sb.k_full[s1], ph1, &sb, p.status)) break;
+        if (lane == 0) {
+          issue_qk(0, s1);
+          mma_commit(&sb.s_full[0]);
+        }
+      }
+      __syncwarp();
+      // Query tile 1: P1 V, then the next S1.
+      if (!wait_warp(&sb.p_full[1], (uint32_t)i & 1u, &sb, p.status)) break;
+      if (lane == 0) {
+        issue_pv(1, s, i == 0);
+        mma_commit(&sb.o_done[1]);
+        mma_commit(&sb.v_empty[s]);
+        if (more) {
+          issue_qk(1, s1);
+          mma_commit(&sb.s_full[1]);
+          mma_commit(&sb.k_empty[s1]);
+        }
+      }
+      __syncwarp();
+    }
+    // Every MMA issued above has completed before TMEM is freed.
+    if (lane == 0 && n_tiles > 0) {
+      mma_commit(&sb.mma_done);
+      drain_bar(&sb.mma_done, 0, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax: one thread per query row ----------------
+    const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + (t ? C::kS1 : C::kS0);
+    const uint32_t o_tm = tmem + lane_off + (t ? C::kO1 : C::kO0);
+    const float sc = p.scale * kLog2e;
+    const bool explicit_x = MASK || !(sc > 0.f);
+    const float c_eff = explicit_x ? 1.f : sc;
+    const float* mrow = nullptr;
+    if (MASK && qrow < p.Sq)
+      mrow = p.M + p.m.off + (int64_t)b * p.m.bs + (int64_t)h * p.m.hs + (int64_t)qrow * p.m.rs;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint32_t x[BN];
+    for (int i = 0; i < n_tiles; ++i) {
+      if (!wait_warp(&sb.s_full[t], (uint32_t)i & 1u, &sb, p.status)) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      const int k0 = (j0 + i) * BN;
+      if (explicit_x) {
+        // Scores to log2 units with the additive mask, one 32-column chunk at a
+        // time (the wait's memory clobber keeps at most 32 mask loads live).
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_ld32(s_tm + c * 32, x + c * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = c * 32; e < c * 32 + 32; ++e) {
+            const int kk = k0 + e;
+            float v = -INFINITY;
+            if (kk >= lo && kk < hi) {
+              const float s = __uint_as_float(x[e]);
+              v = MASK ? fmaf(s, sc, mrow[kk] * kLog2e) : s * sc;
+            }
+            x[e] = __float_as_uint(v);
+            if ((e & 7) == 7) asm volatile("" ::: "memory");  // at most 8 mask loads in flight
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
+        tmem_ld_wait();
+        if (!(k0 >= lo && k0 + BN <= hi)) {
+#pragma unroll
+          for (int e = 0; e < BN; ++e) {
+            const int kk = k0 + e;
+            if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
+          }
+        }
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BN; e += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(x[e]));
+        mx1 = fmaxf(mx1, __uint_as_float(x[e + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(x[e + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(x[e + 3]));
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_eff;
+      const bool raise = mt > m_ref + kSlack;     // also true for the first tile with a visible key
+      float corr = 1.f;
+      if (raise) corr = ex2(m_ref - mt);          // 0 when m_ref = -inf
+      // O holds earlier tiles' sums only if m_ref was finite; it is rescaled
+      // below, after P is stored (warp-uniform TMEM traffic).
+      const bool rescale = raise && m_ref > -INFINITY;
+      if (raise) {
+        l *= corr;
+        m_ref = mt;
+      }
+      const float neg = -(m_ref == -INFINITY ? 0.f : m_ref);
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < BN; e += 2) {
+        const float p0 = ex2(fmaf(__uint_as_float(x[e]), c_eff, neg));
+        const float p1 = ex2(fmaf(__uint_as_float(x[e + 1]), c_eff, neg));
+        ls0 += p0;
+        ls1 += p1;
+        x[e / 2] = pack2<BF16>(p0, p1);
+      }
+      l += ls0 + ls1;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) tmem_st32(s_tm + c * 32, x + c * 32);
+      if (__any_sync(0xffffffffu, rescale)) {
+        // P V of the previous tile must have landed in O before it is scaled.
+        if (!wait_warp(&sb.o_done[t], (uint32_t)(i - 1) & 1u, &sb, p.status)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const float f = rescale ? corr : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_tm + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+          tmem_st32(o_tm + c * 32, o);
+        }
+      }
+      tmem_st_wait();
+      fence_before();
+      mbar_arrive(&sb.p_full[t]);
+    }
+    // ---- epilogue: O / l, special rows, LSE ----
+    if (ok && n_tiles > 0) ok = wait_warp(&sb.o_done[t], (uint32_t)(n_tiles - 1) & 1u, &sb, p.status);
+    if (ok) {
+      fence_after();
+      const bool valid = qrow < p.Sq;
+      const bool hidden_row = (l == 0.f);         // no visible key; a NaN l stays a NaN row
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      T* orow = valid ? static_cast<T*>(p.O) + p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs +
+                            (int64_t)qrow * p.o.rs
+                      : nullptr;
+      const float inv = 1.f / l;
+      const float fill = p.masked_zero ? 0.f : NAN;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(o_tm + c * 32, o);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float a = hidden_row ? fill : __uint_as_float(o[e]) * inv;
+          float bb = hidden_row ? fill : __uint_as_float(o[e + 1]) * inv;
+          w[e / 2] = pack2<BF16>(a, bb);
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+      }
+      if (valid && p.lse)
+        p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
+            hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
+}
+
+// ---- host side -----------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 4-D map over [batch][head][row][element] with a {64 elements, 128 rows} box, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int dtype, int D, int rows, int heads, int batch, const Layout& l) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const char* ptr = static_cast<const char*>(base) + l.off * 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
+  cuuint64_t rs = (cuuint64_t)l.rs * 2, hs = (cuuint64_t)l.hs * 2, bs = (cuuint64_t)l.bs * 2;
+  // A stride is irrelevant when its extent is 1; give it a legal value.
+  if (rows == 1 && rs == 0) rs = 16;
+  if (heads == 1 && hs == 0) hs = 16;
+  if (batch == 1 && bs == 0) bs = 16;
+  cuuint64_t strides[3] = {rs, hs, bs};
+  cuuint32_t box[4] = {64, (cuuint32_t)BM, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                  const_cast<char*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool layout_16b(const void* base, const Layout& l, int rows, int heads, int batch) {
+  if (((uintptr_t)base + (uintptr_t)l.off * 2) % 16) return false;
+  auto ok = [](int64_t stride, int extent) { return extent == 1 || (stride > 0 && (stride * 2) % 16 == 0); };
+  return ok(l.rs, rows) && ok(l.hs, heads) && ok(l.bs, batch) && l.rs * 2 < (1ll << 40) && l.hs * 2 < (1ll << 40) &&
+         l.bs * 2 < (1ll << 40);
+}
+
+template <int D, bool BF16, bool MASK>
+int launch(const Problem& p, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q) || !make_map(&mk, p.K, p.dtype, D, p.Sk, p.G, p.B, p.k) ||
+      !make_map(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v))
+    return -1;  // not describable: caller falls back
+  const int nqb = (p.Sq + 2 * BM - 1) / (2 * BM);
+  const int64_t blocks = (int64_t)nqb * p.H * p.B;
+  if (blocks > 0x7fffffff) return -1;
+  const int smem = Cfg<D>::kSmem + 1024;
+  auto kern = prefill_tc_kernel<D, BF16, MASK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D>
+int launch_d(const Problem& p, cudaStream_t st) {
+  const bool m = p.M != nullptr;
+  if (p.dtype == ATTN_BF16) return m ? launch<D, true, true>(p, st) : launch<D, true, false>(p, st);
+  return m ? launch<D, false, true>(p, st) : launch<D, false, false>(p, st);
+}
+
+}  // namespace tc
+
+int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
+  *used = 0;
+  if (p.dtype != ATTN_BF16 && p.dtype != ATTN_F16) return ATTN_OK;
+  if (p.D != 64 && p.D != 128) return ATTN_OK;
+  if (p.Sk < 1 || p.Sq < 1) return ATTN_OK;
+  if (p.Sk > 0x3fffffff || p.Sq > 0x3fffffff) return ATTN_OK;
+  const float sc = p.scale * tc::kLog2e;
+  if (!(sc == sc) || isinf(sc)) return ATTN_OK;
+  if (!tc::layout_16b(p.Q, p.q, p.Sq, p.H, p.B) || !tc::layout_16b(p.K, p.k, p.Sk, p.G, p.B) ||
+      !tc::layout_16b(p.V, p.v, p.Sk, p.G, p.B) || !tc::layout_16b(p.O, p.o, p.Sq, p.H, p.B))
+    return ATTN_OK;
+  const int rc = p.D == 64 ? tc::launch_d<64>(p, st) : tc::launch_d<128>(p, st);
+  if (rc < 0) return ATTN_OK;  // tensor map refused: generic path
+  *used = 1;
+  return rc;
+}
+
 }  // namespace attn
