@@ -33,7 +33,20 @@ def rng(seed: int, tensor_id: int) -> np.random.Generator:
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bit patterns."""
+    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bit patterns.
+
+    Uses PyTorch's multithreaded CPU conversion when it is importable (the same
+    rounding, checked bit for bit against the numpy form in the tests)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    try:
+        import torch
+    except ImportError:
+        return f32_to_bf16_bits_numpy(x)
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def f32_to_bf16_bits_numpy(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty(x.shape, dtype=np.uint16)
     flat_in = x.reshape(-1)

@@ -501,3 +501,15 @@ def test_oracle_rejects_bad_problems():
     prob["kv_heads"] = 3
     with pytest.raises(ValueError):
         oracle.attn(prob, qs, ks, vs, rows=np.array([[0, 3, 0]]))
+
+
+def test_bf16_rounding_paths_agree_bit_for_bit():
+    r = np.random.default_rng(77)
+    x = (r.standard_normal(1 << 16) * np.exp(r.uniform(-30, 30, 1 << 16))).astype(np.float32)
+    x[:4] = [np.inf, -np.inf, 0.0, -0.0]
+    # ties: values exactly halfway between two bfloat16 numbers
+    x[4:8] = np.array([0x3F808000, 0x3F818000, 0xBF808000, 0x00008000], dtype=np.uint32).view(np.float32)
+    a = wl.f32_to_bf16_bits(x)
+    b = wl.f32_to_bf16_bits_numpy(x)
+    assert np.array_equal(a, b)
+    assert list(a[4:8]) == [0x3F80, 0x3F82, 0xBF80, 0x0000]
