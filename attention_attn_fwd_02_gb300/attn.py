@@ -22,7 +22,8 @@ ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = 4, 5, 6
 ATTN_OFFSET_DEFAULT = -(2**63)
 DTYPE_CODE = {"f32": ATTN_F32, "f16": ATTN_F16, "bf16": ATTN_BF16}
 EXPORTS = ("attn_fwd_workspace_size", "attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_combine",
-           "attn_device_status", "attn_status_string", "attn_version")
+           "attn_device_status", "attn_status_string", "attn_version", "attn_decode_noalloc",
+           "attn_decode_noalloc_max_scratch")
 
 
 class attn_layout(ctypes.Structure):
@@ -70,6 +71,9 @@ def lib():
         L.attn_device_status.argtypes, L.attn_device_status.restype = [vp], ctypes.c_int
         L.attn_status_string.argtypes, L.attn_status_string.restype = [ctypes.c_int], ctypes.c_char_p
         L.attn_version.argtypes, L.attn_version.restype = [], ctypes.c_int
+        L.attn_decode_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.attn_decode_noalloc.restype = ctypes.c_int
+        L.attn_decode_noalloc_max_scratch.argtypes, L.attn_decode_noalloc_max_scratch.restype = [], sz
         _lib = L
     return _lib
 
@@ -92,6 +96,16 @@ def attn_fwd(p, q, k, v, o, mask, seg, k_lens, lse, workspace, workspace_bytes, 
 def attn_decode(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse, workspace, workspace_bytes, stream) -> int:
     return lib().attn_decode(ctypes.byref(p), q, k_cache, v_cache, o, mask, seg, k_lens, lse, workspace,
                              workspace_bytes, stream)
+
+
+def attn_decode_noalloc(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse, stream) -> int:
+    """attn_decode with the library's fixed device scratch array instead of a caller workspace,
+    for callers that cannot allocate device memory (see include/attn.h)."""
+    return lib().attn_decode_noalloc(ctypes.byref(p), q, k_cache, v_cache, o, mask, seg, k_lens, lse, stream)
+
+
+def attn_decode_noalloc_max_scratch() -> int:
+    return lib().attn_decode_noalloc_max_scratch()
 
 
 def attn_combine(n_splits, rows, head_dim, part_o, part_lse, out_dtype, o, o_row_stride, lse, masked_rows,

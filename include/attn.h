@@ -143,6 +143,27 @@ ATTN_API int attn_decode(const attn_problem* p, const void* q, const void* k_cac
                 void* o, const float* mask, const int32_t* seg, const int32_t* k_lens, float* lse,
                 void* workspace, size_t workspace_bytes, attn_stream stream);
 
+/* attn_decode without a caller workspace, for callers that cannot allocate
+ * device memory (code handed only a stream, allocator hooks, loops that must
+ * not take allocator locks, plugins of a runtime that owns all device memory).
+ * The pages describe no such entry point; it is an addition of this library.
+ * Same arguments and results as attn_decode minus the workspace: the partial
+ * results live in a fixed device array of attn_decode_noalloc_max_scratch()
+ * bytes (32 MiB) that this library holds on every GPU it is loaded on until
+ * the process exits.  A problem whose attn_decode_workspace_size exceeds that
+ * returns ATTN_ERR_WORKSPACE and launches nothing.  The first call on a device
+ * looks up the array's device address (once per device); make it before any
+ * stream capture.  No call allocates or frees memory.  All calls share the
+ * array: calls whose GPU work overlaps (different streams or host threads)
+ * race, so serialise them.  The array keeps the last call's contents; every
+ * value a call reads was written by that call. */
+ATTN_API int attn_decode_noalloc(const attn_problem* p, const void* q, const void* k_cache,
+                                 const void* v_cache, void* o, const float* mask, const int32_t* seg,
+                                 const int32_t* k_lens, float* lse, attn_stream stream);
+
+/* Size in bytes of the fixed scratch array attn_decode_noalloc uses. */
+ATTN_API size_t attn_decode_noalloc_max_scratch(void);
+
 /* Merge per-range partial results of `rows` rows ("Attention", section
  * "Accuracy at long key lengths": partials merged in range order).
  * part_o: float32 [rows][n_splits][head_dim], each already divided by its own
