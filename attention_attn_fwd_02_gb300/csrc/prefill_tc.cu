@@ -29,14 +29,12 @@
 // library status word (ATTN_ERR_DEVICE_TIMEOUT); every role then leaves its
 // loop, waits (bounded) for its own copies and MMAs in flight, and the TMEM
 // owner frees TMEM before the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <string.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "prefill_tc.h"
+#include "tma.h"
 
 namespace attn {
 namespace tc {
@@ -589,53 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -----------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 4-D map over [batch][head][row][element] with a {64 elements, 128 rows} box, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int dtype, int D, int rows, int heads, int batch, const Layout& l) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const char* ptr = static_cast<const char*>(base) + l.off * 2;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
-  cuuint64_t rs = (cuuint64_t)l.rs * 2, hs = (cuuint64_t)l.hs * 2, bs = (cuuint64_t)l.bs * 2;
-  // A stride is irrelevant when its extent is 1; give it a legal value.
-  if (rows == 1 && rs == 0) rs = 16;
-  if (heads == 1 && hs == 0) hs = 16;
-  if (batch == 1 && bs == 0) bs = 16;
-  cuuint64_t strides[3] = {rs, hs, bs};
-  cuuint32_t box[4] = {64, (cuuint32_t)BM, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
-                  const_cast<char*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-bool layout_16b(const void* base, const Layout& l, int rows, int heads, int batch) {
-  if (((uintptr_t)base + (uintptr_t)l.off * 2) % 16) return false;
-  auto ok = [](int64_t stride, int extent) { return extent == 1 || (stride > 0 && (stride * 2) % 16 == 0); };
-  return ok(l.rs, rows) && ok(l.hs, heads) && ok(l.bs, batch) && l.rs * 2 < (1ll << 40) && l.hs * 2 < (1ll << 40) &&
-         l.bs * 2 < (1ll << 40);
-}
-
 template <int D, bool BF16, bool MASK>
 int launch(const Problem& p, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q) || !make_map(&mk, p.K, p.dtype, D, p.Sk, p.G, p.B, p.k) ||
-      !make_map(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v))
+  if (!tma_map_bhsd(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q, BM) ||
+      !tma_map_bhsd(&mk, p.K, p.dtype, D, p.Sk, p.G, p.B, p.k, BN) ||
+      !tma_map_bhsd(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v, BN))
     return -1;  // not describable: caller falls back
   const int nqb = (p.Sq + 2 * BM - 1) / (2 * BM);
   const int64_t blocks = (int64_t)nqb * p.H * p.B;
@@ -665,8 +622,8 @@ int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
   if (p.Sk > 0x3fffffff || p.Sq > 0x3fffffff) return ATTN_OK;
   const float sc = p.scale * tc::kLog2e;
   if (!(sc == sc) || isinf(sc)) return ATTN_OK;
-  if (!tc::layout_16b(p.Q, p.q, p.Sq, p.H, p.B) || !tc::layout_16b(p.K, p.k, p.Sk, p.G, p.B) ||
-      !tc::layout_16b(p.V, p.v, p.Sk, p.G, p.B) || !tc::layout_16b(p.O, p.o, p.Sq, p.H, p.B))
+  if (!tma_layout_ok(p.Q, p.q, p.Sq, p.H, p.B) || !tma_layout_ok(p.K, p.k, p.Sk, p.G, p.B) ||
+      !tma_layout_ok(p.V, p.v, p.Sk, p.G, p.B) || !tma_layout_ok(p.O, p.o, p.Sq, p.H, p.B))
     return ATTN_OK;
   const int rc = p.D == 64 ? tc::launch_d<64>(p, st) : tc::launch_d<128>(p, st);
   if (rc < 0) return ATTN_OK;  // tensor map refused: generic path
