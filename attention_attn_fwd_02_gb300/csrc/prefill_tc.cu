@@ -217,6 +217,29 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// Packed pair arithmetic (f32x2) and a three-input maximum: half the issue
+// slots of the scalar forms for the softmax's per-element work.
+__device__ __forceinline__ uint64_t f2u(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a0, a1)), "l"(b), "l"(c));
+  d0 = __uint_as_float((uint32_t)d);
+  d1 = __uint_as_float((uint32_t)(d >> 32));
+}
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a0, a1)), "l"(f2u(b0, b1)));
+  a0 = __uint_as_float((uint32_t)d);
+  a1 = __uint_as_float((uint32_t)(d >> 32));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int D>
 struct Cfg {
   static constexpr int kChunks = D / 64;                  // 64-column (128-byte) chunks
@@ -482,15 +505,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int e = 0; e < BN; e += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(x[e]));
-        mx1 = fmaxf(mx1, __uint_as_float(x[e + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(x[e + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(x[e + 3]));
+        mx0 = max3(mx0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+        mx1 = max3(mx1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_eff;
+      const float mt = fmaxf(mx0, mx1) * c_eff;
       const bool raise = mt > m_ref + kSlack;     // also true for the first tile with a visible key
       float corr = 1.f;
       if (raise) corr = ex2(m_ref - mt);          // 0 when m_ref = -inf
@@ -502,16 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = mt;
       }
       const float neg = -(m_ref == -INFINITY ? 0.f : m_ref);
-      float ls0 = 0.f, ls1 = 0.f;
+      const uint64_t c2 = f2u(c_eff, c_eff), n2 = f2u(neg, neg);
+      float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < BN; e += 2) {
-        const float p0 = ex2(fmaf(__uint_as_float(x[e]), c_eff, neg));
-        const float p1 = ex2(fmaf(__uint_as_float(x[e + 1]), c_eff, neg));
-        ls0 += p0;
-        ls1 += p1;
-        x[e / 2] = pack2<BF16>(p0, p1);
+      for (int e = 0; e < BN; e += 4) {
+        float a0, a1, b0, b1;
+        fma2(a0, a1, __uint_as_float(x[e]), __uint_as_float(x[e + 1]), c2, n2);
+        fma2(b0, b1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]), c2, n2);
+        a0 = ex2(a0);
+        a1 = ex2(a1);
+        b0 = ex2(b0);
+        b1 = ex2(b1);
+        add2(la0, la1, a0, a1);
+        add2(lb0, lb1, b0, b1);
+        x[e / 2] = pack2<BF16>(a0, a1);
+        x[e / 2 + 1] = pack2<BF16>(b0, b1);
       }
-      l += ls0 + ls1;
+      l += (la0 + la1) + (lb0 + lb1);
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) tmem_st32(s_tm + c * 32, x + c * 32);
       if (__any_sync(0xffffffffu, rescale)) {

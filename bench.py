@@ -236,7 +236,7 @@ def run_ours(args):
     L = attn.lib()
 
     pf = wl.long_causal_gqa_bf16()
-    dc = wl.decode_bnsh_bf16()
+    dc = wl.decode_bnsh_bf16(batch=args.decode_batch)
     P = pf.problem
     D = P["head_dim"]
     pairs = wl.visible_pairs(pf)
@@ -266,6 +266,8 @@ def run_ours(args):
     dprob = attn.make_problem(dP)
     ws_bytes = attn.attn_decode_workspace_size(dprob)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    pws_bytes = attn.attn_fwd_workspace_size(pprob)
+    pws = torch.empty(max(pws_bytes, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     st = stream.cuda_stream
@@ -274,7 +276,7 @@ def run_ours(args):
         if args.only == "decode":
             return
         rc = attn.attn_fwd(pprob, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, None, kl.data_ptr(),
-                           lse.data_ptr(), None, 0, st)
+                           lse.data_ptr(), pws.data_ptr() if pws_bytes else None, pws_bytes, st)
         if rc:
             raise attn.AttnError(rc, "attn_fwd")
 
@@ -438,6 +440,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--decode-batch", type=int, default=64,
+                    help="batch of the decode workload (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one half of the step only (for profiling); the line is then partial")
     args = ap.parse_args()
