@@ -414,8 +414,9 @@ def run_ours(args):
         "config": {"workload": f"{pf.name} + {dc.name}", "prefill": pf.name, "decode": dc.name,
                    "visible_pairs": pairs, "decode_kv_bytes": kv_bytes, "l2": "flushed (256 MiB write) between steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roof,
-        "decode": {"value": dec_gbs, "unit": "GB/s", "ms_per_step": 1e3 * dec_s / steps, "roofline": dec_roof},
+        "roofline": None if args.only == "decode" else roof,
+        "decode": (None if args.only == "prefill" else
+               {"value": dec_gbs, "unit": "GB/s", "ms_per_step": 1e3 * dec_s / steps, "roofline": dec_roof}),
         "prefill_ms_per_step": 1e3 * pre_s / steps,
         "cpu_baseline": cpu,
         "e2e": e2e,
