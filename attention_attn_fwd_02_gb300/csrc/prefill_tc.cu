@@ -34,6 +34,7 @@
 #include <type_traits>
 
 #include "prefill_tc.h"
+#include "tc_ptx.cuh"
 #include "tma.h"
 
 namespace attn {
@@ -42,7 +43,6 @@ namespace tc {
 constexpr int BM = 128;            // query rows per tile
 constexpr int BN = 128;            // keys per tile
 constexpr int kThreads = 320;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kSlack = 8.0f;     // log2 units
@@ -56,189 +56,6 @@ struct Bars {
   int abort;
   int lo_u, hi_u;
 };
-
-// ---- PTX wrappers ------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `b` with parity `parity`.
-__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, Bars* sb, int* status) {
-  if (mbar_try(b, parity)) return true;
-  const uint64_t t0 = gtimer();
-  while (!mbar_try(b, parity)) {
-    if (*(volatile int*)&sb->abort) return false;
-    if (gtimer() - t0 > kTimeoutNs) {
-      *(volatile int*)&sb->abort = 1;
-      atomicExch(status, ATTN_ERR_DEVICE_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
-// Teardown wait: bounded, does not look at the abort flag.
-__device__ __forceinline__ bool drain_bar(uint64_t* b, uint32_t parity, int* status) {
-  const uint64_t t0 = gtimer();
-  while (!mbar_try(b, parity)) {
-    if (gtimer() - t0 > kTimeoutNs) {
-      atomicExch(status, ATTN_ERR_DEVICE_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
-// Warp-uniform bounded wait: every lane waits, and the warp proceeds only if
-// all lanes saw the phase complete, so warp-collective TMEM instructions that
-// follow never run with part of the warp.
-__device__ __forceinline__ bool wait_warp(uint64_t* b, uint32_t parity, Bars* sb, int* status) {
-  const bool ok = wait_bar(b, parity, sb, status);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
-                                            int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t* b) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
-               : "memory");
-}
-
-#define ATTN_R32(r)                                                                                                 \
-  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),       \
-      "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),        \
-      "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),       \
-      "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-#define ATTN_W32(r)                                                                                                 \
-  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),    \
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),   \
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),   \
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-
-// 32 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : ATTN_R32(r)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      ATTN_W32(r)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start,
-// leading and stride byte offsets in 16-byte units, descriptor version 1).
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// Instruction descriptor, kind::f16 with f32 accumulation.
-__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-}
-
-// Packed pair arithmetic (f32x2) and a three-input maximum: half the issue
-// slots of the scalar forms for the softmax's per-element work.
-__device__ __forceinline__ uint64_t f2u(float lo, float hi) {
-  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a0, a1)), "l"(b), "l"(c));
-  d0 = __uint_as_float((uint32_t)d);
-  d1 = __uint_as_float((uint32_t)(d >> 32));
-}
-__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a0, a1)), "l"(f2u(b0, b1)));
-  a0 = __uint_as_float((uint32_t)d);
-  a1 = __uint_as_float((uint32_t)(d >> 32));
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
 
 template <int D>
 struct Cfg {
@@ -334,11 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i % C::kStages;
         const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
         const int krow = (j0 + i) * BN;
-        if (!wait_bar(&sb.k_empty[s], ph ^ 1u, &sb, p.status)) break;
+        if (!wait_bar(&sb.k_empty[s], ph ^ 1u, &sb.abort, p.status)) break;
         mbar_expect_tx(&sb.k_full[s], C::kKTile);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(k_s + s * C::kKTile + c * BN * 128, &tm_k, &sb.k_full[s], c * 64, krow, g, b);
-        if (!wait_bar(&sb.v_empty[s], ph ^ 1u, &sb, p.status)) {
+        if (!wait_bar(&sb.v_empty[s], ph ^ 1u, &sb.abort, p.status)) {
           k_only = i;
           break;
         }
@@ -365,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdPV = idesc_f16(BF16, true, BM, D);
     const uint32_t q_addr = su32(q_s), k_addr = su32(k_s), v_addr = su32(v_s);
     bool ok = n_tiles > 0;
-    if (ok) ok = wait_warp(&sb.q_full, 0, &sb, p.status);
+    if (ok) ok = wait_warp(&sb.q_full, 0, &sb.abort, p.status);
     auto issue_qk = [&](int tt, int s) {
       fence_after();
 #pragma unroll
@@ -386,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     // Prologue: S0 and S1 of tile 0.
-    if (ok) ok = wait_warp(&sb.k_full[0], 0, &sb, p.status);
+    if (ok) ok = wait_warp(&sb.k_full[0], 0, &sb.abort, p.status);
     if (ok && lane == 0) {
       issue_qk(0, 0);
       mma_commit(&sb.s_full[0]);
@@ -399,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = i % C::kStages;
       const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
       const int k0 = (j0 + i) * BN;
-      if (!wait_warp(&sb.v_full[s], ph, &sb, p.status)) break;
+      if (!wait_warp(&sb.v_full[s], ph, &sb.abort, p.status)) break;
       // Zero the V rows of keys no row of this CTA sees (they may hold anything).
       if (k0 < lo_u || k0 + BN > hi_u) {
         for (int u = lane; u < BN * C::kChunks * 8; u += 32) {
@@ -419,14 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s1 = (i + 1) % C::kStages;
       const uint32_t ph1 = (uint32_t)((i + 1) / C::kStages) & 1u;
       // Query tile 0: P0 V, then the next S0.
-      if (!wait_warp(&sb.p_full[0], (uint32_t)i & 1u, &sb, p.status)) break;
+      if (!wait_warp(&sb.p_full[0], (uint32_t)i & 1u, &sb.abort, p.status)) break;
       if (lane == 0) {
         issue_pv(0, s, i == 0);
         mma_commit(&sb.o_done[0]);
       }
       __syncwarp();
       if (more) {
-        if (!wait_warp(&sb.k_full[s1], ph1, &sb, p.status)) break;
+        if (!wait_warp(&sb.k_full[s1], ph1, &sb.abort, p.status)) break;
         if (lane == 0) {
           issue_qk(0, s1);
           mma_commit(&sb.s_full[0]);
@@ -434,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       // Query tile 1: P1 V, then the next S1.
-      if (!wait_warp(&sb.p_full[1], (uint32_t)i & 1u, &sb, p.status)) break;
+      if (!wait_warp(&sb.p_full[1], (uint32_t)i & 1u, &sb.abort, p.status)) break;
       if (lane == 0) {
         issue_pv(1, s, i == 0);
         mma_commit(&sb.o_done[1]);
@@ -468,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t x[BN];
     for (int i = 0; i < n_tiles; ++i) {
-      if (!wait_warp(&sb.s_full[t], (uint32_t)i & 1u, &sb, p.status)) {
+      if (!wait_warp(&sb.s_full[t], (uint32_t)i & 1u, &sb.abort, p.status)) {
         ok = false;
         break;
       }
@@ -544,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < BN / 64; ++c) tmem_st32(s_tm + c * 32, x + c * 32);
       if (__any_sync(0xffffffffu, rescale)) {
         // P V of the previous tile must have landed in O before it is scaled.
-        if (!wait_warp(&sb.o_done[t], (uint32_t)(i - 1) & 1u, &sb, p.status)) {
+        if (!wait_warp(&sb.o_done[t], (uint32_t)(i - 1) & 1u, &sb.abort, p.status)) {
           ok = false;
           break;
         }
@@ -565,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sb.p_full[t]);
     }
     // ---- epilogue: O / l, special rows, LSE ----
-    if (ok && n_tiles > 0) ok = wait_warp(&sb.o_done[t], (uint32_t)(n_tiles - 1) & 1u, &sb, p.status);
+    if (ok && n_tiles > 0) ok = wait_warp(&sb.o_done[t], (uint32_t)(n_tiles - 1) & 1u, &sb.abort, p.status);
     if (ok) {
       fence_after();
       const bool valid = qrow < p.Sq;
@@ -645,7 +462,7 @@ int launch_d(const Problem& p, cudaStream_t st) {
 int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
   *used = 0;
   if (p.dtype != ATTN_BF16 && p.dtype != ATTN_F16) return ATTN_OK;
-  if (p.D != 64 && p.D != 128) return ATTN_OK;
+  if (p.D != 64 && p.D != 128 && p.D != 256) return ATTN_OK;
   if (p.Sk < 1 || p.Sq < 1) return ATTN_OK;
   if (p.Sk > 0x3fffffff || p.Sq > 0x3fffffff) return ATTN_OK;
   const float sc = p.scale * tc::kLog2e;
@@ -653,7 +470,7 @@ int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
   if (!tma_layout_ok(p.Q, p.q, p.Sq, p.H, p.B) || !tma_layout_ok(p.K, p.k, p.Sk, p.G, p.B) ||
       !tma_layout_ok(p.V, p.v, p.Sk, p.G, p.B) || !tma_layout_ok(p.O, p.o, p.Sq, p.H, p.B))
     return ATTN_OK;
-  const int rc = p.D == 64 ? tc::launch_d<64>(p, st) : tc::launch_d<128>(p, st);
+  const int rc = p.D == 256 ? prefill_tc1_launch(p, st) : (p.D == 64 ? tc::launch_d<64>(p, st) : tc::launch_d<128>(p, st));
   if (rc < 0) return ATTN_OK;  // tensor map refused: generic path
   *used = 1;
   return rc;

@@ -7,4 +7,8 @@ namespace attn {
 // head_dim it is built for, a layout TMA can describe).  Sets *used = 1 when
 // it launched; returns an ATTN_* status.
 int prefill_tc_try(const Problem& p, cudaStream_t st, int* used);
+
+// The head_dim 256 kernel (one query tile per CTA, double-buffered S).
+// Returns -1 when TMA cannot describe the layout, else an ATTN_* status.
+int prefill_tc1_launch(const Problem& p, cudaStream_t st);
 }  // namespace attn
