@@ -257,21 +257,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after();
       const int k0 = (j0 + i) * BN;
       if (explicit_x) {
+        // Scores to log2 units plus the additive mask.  A whole in-range,
+        // 16-byte-aligned mask slice is read with vector loads.
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          tmem_ld32(s_tm + c * 32, x + c * 32);
-          tmem_ld_wait();
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
+        float mv[BN];
+        if (MASK) {
+          const float* mp = mrow ? mrow + k0 : nullptr;
+          if (mp && k0 + BN <= p.Sk && ((uintptr_t)mp & 15) == 0) {
 #pragma unroll
-          for (int e = c * 32; e < c * 32 + 32; ++e) {
-            const int kk = k0 + e;
-            float v = -INFINITY;
-            if (kk >= lo && kk < hi) {
-              const float s = __uint_as_float(x[e]);
-              v = MASK ? fmaf(s, sc, mrow[kk] * kLog2e) : s * sc;
+            for (int j = 0; j < BN / 4; ++j) {
+              const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
+              mv[4 * j] = v4.x;
+              mv[4 * j + 1] = v4.y;
+              mv[4 * j + 2] = v4.z;
+              mv[4 * j + 3] = v4.w;
             }
-            x[e] = __float_as_uint(v);
-            if ((e & 7) == 7) asm volatile("" ::: "memory");  // at most 8 mask loads in flight
+          } else {
+#pragma unroll
+            for (int e = 0; e < BN; ++e) mv[e] = (mp && k0 + e >= lo && k0 + e < hi) ? mp[e] : 0.f;
           }
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const int kk = k0 + e;
+          const float s = __uint_as_float(x[e]);
+          const float v = MASK ? fmaf(s, sc, mv[e] * kLog2e) : s * sc;
+          x[e] = __float_as_uint((kk >= lo && kk < hi) ? v : -INFINITY);
         }
       } else {
 #pragma unroll
