@@ -60,6 +60,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise maximum of per-rank timings (seconds) over all ranks.
+
+    The path has no exchange step, so ranks are independent replicas: the
+    whole job finishes when the slowest rank does."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(units_per_rank: float, world: int, steps: int, slowest_seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return world * steps * units_per_rank / slowest_seconds
+
+
 def decode_kv_bytes(case) -> int:
     p = case.problem
     kl = np.clip(case.k_lens.astype(np.int64), 0, p["k_len"])
@@ -339,15 +357,12 @@ def run_ours(args):
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [a + b for a, b in zip(pre_ms, dec_ms)]
-    tot = torch.tensor([sum(pre_ms), sum(dec_ms), sum(step_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
-    pre_s, dec_s, step_s = (float(x) / 1e3 for x in tot.cpu())
+    pre_s, dec_s, step_s = max_over_ranks([sum(pre_ms) / 1e3, sum(dec_ms) / 1e3, sum(step_ms) / 1e3], world, dev)
     steps = args.steps
     pre_s = max(pre_s, 1e-12)
     dec_s = max(dec_s, 1e-12)
-    value = world * steps * flops / pre_s / 1e12
-    dec_gbs = world * steps * kv_bytes / dec_s / 1e9
+    value = job_throughput(flops, world, steps, pre_s) / 1e12
+    dec_gbs = job_throughput(kv_bytes, world, steps, dec_s) / 1e9
 
     # e2e through the public API with pinned host buffers
     e2e = None
@@ -381,14 +396,12 @@ def run_ours(args):
             e2e_step()
             ee[s][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = torch.tensor([sum(a.elapsed_time(b) for a, b in ee)], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(e_ms, op=torch.distributed.ReduceOp.MAX)
-        e2e = {"value": world * steps * flops / (float(e_ms.item()) / 1e3) / 1e12, "unit": "TFLOP/s",
+        (e_s,) = max_over_ranks([sum(a.elapsed_time(b) for a, b in ee) / 1e3], world, dev)
+        e2e = {"value": job_throughput(flops, world, steps, e_s) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     pk, pk_kind = peaks()
-    digest = source_digest("prefill_tc.cu")
+    digest = source_digest("prefill_tc.cu", "tc_ptx.cuh")
     pre_launch_s = pre_s / steps
     roof = {"bound": "tensor", "achieved": flops / pre_launch_s / 1e12, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": flops / pre_launch_s / 1e12 / pk["bf16_tflops"],
