@@ -127,26 +127,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp < 8 && hi > lo) {
-    atomicMin(&sb.lo_u, lo);
-    atomicMax(&sb.hi_u, hi);
+  // Q does not depend on the key range: its copy starts at once.
+  if (threadIdx.x == 8 * 32) {
+    mbar_expect_tx(&sb.q_full, 2 * C::kQTile);
+    for (int tt = 0; tt < 2; ++tt)
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
   }
-  __syncthreads();
+  // The union of the rows' visible key ranges.  Without segment starts every
+  // range begins at key 0 and ends at a bound that does not decrease with the
+  // row, so the last valid row gives the union; otherwise reduce over rows.
+  int lo_u, hi_u;
+  if (p.seg == nullptr) {
+    const int last = min(q0 + 2 * BM, p.Sq) - 1;
+    int64_t l64 = 0, h64 = 0;
+    if (last >= q0) row_range(p, b, last, l64, h64);
+    lo_u = 0;
+    hi_u = h64 > 0 ? (int)h64 : -1;
+  } else {
+    if (warp < 8 && hi > lo) {
+      atomicMin(&sb.lo_u, lo);
+      atomicMax(&sb.hi_u, hi);
+    }
+    __syncthreads();
+    lo_u = sb.lo_u;
+    hi_u = sb.hi_u;
+  }
   const uint32_t tmem = sb.tmem_base;
-  const int lo_u = sb.lo_u, hi_u = sb.hi_u;
   const bool any = hi_u > lo_u;
   const int j0 = any ? lo_u / BN : 0;
   const int n_tiles = any ? (hi_u + BN - 1) / BN - j0 : 0;
 
   if (warp == 8) {
     // ---------------- TMA producer ----------------
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       int issued = 0;          // tiles whose K and V copies were both issued
       int k_only = -1;         // a tile whose K copy was issued but not its V copy
-      mbar_expect_tx(&sb.q_full, 2 * C::kQTile);
-      for (int tt = 0; tt < 2; ++tt)
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % C::kStages;
         const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
