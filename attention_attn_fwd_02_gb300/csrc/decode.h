@@ -4,7 +4,7 @@
 
 namespace attn {
 // Launches the specialised decode split pass when the problem fits it
-// (f16/bf16, head_dim 64 or 128, contiguous 16-byte-aligned cache rows).
+// (f16/bf16, head_dim 128, a cache layout TMA can describe).
 // Sets *used = 1 when it launched; returns an ATTN_* status.
 int decode_fast_try(const Problem& p, const Split& s, cudaStream_t st, int* used);
 }  // namespace attn

@@ -234,3 +234,50 @@ def test_prefill_without_workspace_uses_static_schedule():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
     ref_o, ref_l = oracle_full(c)
     compare(o, l2, ref_o, ref_l, "bf16", "nan", "static schedule")
+
+
+# ---- decode variants (the tensor-core split pass and the generic one) ---------------------
+
+DECODE = [
+    # dtype, B, H, G, cap, D, mask, lse, lens
+    ("bf16", 3, 16, 16, 1000, 128, False, True, "rand"),     # one query head per kv head
+    ("f16", 2, 10, 5, 777, 128, True, True, "rand"),         # 2 heads per group, mask, f16
+    ("bf16", 2, 16, 1, 1300, 128, False, False, "zero_full"),  # 16 heads per group, lengths 0 and cap
+    ("bf16", 1, 40, 2, 600, 128, True, True, "rand"),        # 20 heads per group: two head chunks
+    ("bf16", 2, 8, 2, 900, 64, False, True, "rand"),         # head_dim 64: generic split pass
+    ("f16", 2, 6, 3, 513, 96, True, True, None),             # head_dim 96, no lengths: generic
+]
+
+
+@pytest.mark.parametrize("i", range(len(DECODE)))
+def test_decode_variants(i):
+    dtype, B, H, G, cap, D, use_mask, lse, lens = DECODE[i]
+    r = np.random.default_rng(500 + i)
+    k_lens = None
+    if lens == "rand":
+        k_lens = r.integers(1, cap + 1, size=B).astype(np.int32)
+    elif lens == "zero_full":
+        k_lens = np.array([0, cap], dtype=np.int32)
+    mask = None
+    if use_mask:
+        mask = r.standard_normal((B, 1, 1, cap)).astype(np.float32)
+        mask[r.random(mask.shape) < 0.15] = -np.inf
+    c = wl.make_case(name=f"decode{i}", seed=600 + i, dtype=dtype, batch=B, heads=H, kv_heads=G, q_len=1,
+                     k_len=cap, head_dim=D, k_lens=k_lens, mask=mask, mask_kind="b11k", decode=True)
+    st, _ = run_and_compare(c, lse=lse)
+    if lens == "zero_full":
+        assert st["nan_rows"] == H      # batch entry 0 has no valid key
+
+
+def test_decode_bounded_wait_reports_timeout_and_context_stays_usable(monkeypatch):
+    """A stage copy that never lands makes the split pass's bounded waits run
+    out: the kernel records ATTN_ERR_DEVICE_TIMEOUT and exits; the next call on
+    the same context is correct."""
+    c = wl.decode_bnsh_bf16(seed=77, batch=2, capacity=1024, heads=8, kv_heads=2, min_len=600)
+    monkeypatch.setenv("ATTN_TEST_DROP_FIRST_COPY", "1")
+    g = GpuCase(c).run()
+    torch_mod().cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_ERR_DEVICE_TIMEOUT
+    monkeypatch.delenv("ATTN_TEST_DROP_FIRST_COPY")
+    assert attn.attn_device_status() == attn.ATTN_OK      # the status word was cleared
+    run_and_compare(c)
