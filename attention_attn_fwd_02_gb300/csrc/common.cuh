@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "attn.h"
 
 namespace attn {
@@ -72,6 +74,32 @@ __device__ __forceinline__ void row_range(const Problem& p, int b, int i, int64_
   }
   lo = 0;
   if (p.seg) lo = clamp64((int64_t)p.seg[(int64_t)b * p.seg_bs + i], 0, p.Sk);
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device once; the setting lasts for the process, so later launches only look
+// it up (the attribute call costs microseconds, which small problems feel).
+inline cudaError_t ensure_smem(const void* kern, int bytes) {
+  struct Entry {
+    const void* k;
+    int dev, bytes;
+  };
+  static std::mutex mu;
+  static Entry tab[256];
+  static int n = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+      if (tab[i].k == kern && tab[i].dev == dev && tab[i].bytes >= bytes) return cudaSuccess;
+  }
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (n < 256) tab[n++] = {kern, dev, bytes};
+  }
+  return e;
 }
 
 // Host-side launchers (defined in the kernel translation units).

@@ -427,7 +427,7 @@ int launch_mma(const Problem& p, const Split& s, cudaStream_t st) {
   if (blocks <= 0 || blocks > 0x7fffffff) return -1;
   const int smem = kMStages * 2 * kMTile + 1024;
   auto kern = decode_mma_kernel<BF16>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (ensure_smem((const void*)kern, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const char* drop = getenv("ATTN_TEST_DROP_FIRST_COPY");
   kern<<<(unsigned)blocks, kThreads, smem, st>>>(mk, mv, p, s, n_hc, drop && drop[0] == '1' ? 1 : 0);

@@ -415,7 +415,7 @@ int launch(const Problem& p, cudaStream_t st) {
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D>::kSmem + 1024;
   auto kern = prefill_tc1_kernel<D, BF16, MASK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

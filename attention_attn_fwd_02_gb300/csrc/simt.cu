@@ -237,8 +237,7 @@ cudaError_t launch_simt_t(const Problem& p, const Split& s, cudaStream_t st) {
   if (blocks <= 0) return cudaSuccess;
   if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)2 * kTile * p.D * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(simt_attn_kernel<T, TPR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = ensure_smem((const void*)simt_attn_kernel<T, TPR>, (int)smem);
   if (e != cudaSuccess) return e;
   simt_attn_kernel<T, TPR><<<(unsigned)blocks, kThreads, smem, st>>>(p, s, row_blocks);
   return cudaGetLastError();
