@@ -13,11 +13,16 @@
 // from section "Matrix hardware": the probabilities are rounded to the element
 // type before the P V product.
 //
-// CTA: 320 threads, two 128-row query tiles (256 rows) of one (batch, head).
+// CTA: 384 threads (three warpgroups), two 128-row query tiles (256 rows) of
+// one (batch, head).
 //   warps 0-3  softmax for query tile 0 (thread = one row = one TMEM lane)
 //   warps 4-7  softmax for query tile 1
 //   warp 8     TMA producer (Q once, then K and V tiles through a ring)
 //   warp 9     TMEM owner and MMA issuer (one elected lane issues)
+//   warps 10-11 idle: they complete the third warpgroup so that it can hand
+//              its registers to the softmax warpgroups (setmaxnreg: 216 per
+//              softmax thread, which holds a 128-column row of S without
+//              spilling, and 56 per producer thread)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after them; the
 // probabilities P overwrite the first BN/2 columns of their S tile as packed
 // 16-bit pairs and feed the second MMA straight from TMEM.
@@ -42,7 +47,14 @@ namespace tc {
 
 constexpr int BM = 128;            // query rows per tile
 constexpr int BN = 128;            // keys per tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // softmax warpgroups 0-1, producer warpgroup 2 (TMA warp, MMA warp, two idle)
+// Per-thread registers after the split.  The block is launched with 168
+// (65536 / 384, rounded down to the allocation unit); 8 warps x 216 plus
+// 4 warps x 56 is 62464 <= 384 x 168 = 64512, so the increase never waits.
+constexpr int kSoftmaxRegs = 216;
+constexpr int kProducerRegs = 56;
+constexpr int kSplitRegs = 8 * 32 * kSoftmaxRegs + 4 * 32 * kProducerRegs;
+static_assert(kSplitRegs <= kThreads * ((65536 / kThreads) & ~7), "register split exceeds the block's registers");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kSlack = 8.0f;     // log2 units
@@ -158,7 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j0 = any ? lo_u / BN : 0;
   const int n_tiles = any ? (hi_u + BN - 1) / BN - j0 : 0;
 
+  // Registers move from the producer warpgroup to the softmax warpgroups.
+  // Each role sets its own count inside its branch, so no code after the
+  // change is compiled under both limits.
   if (warp == 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       int issued = 0;          // tiles whose K and V copies were both issued
@@ -193,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k_only >= 0) drain_bar(&sb.k_full[k_only % C::kStages], (uint32_t)(k_only / C::kStages) & 1u, p.status);
     }
   } else if (warp == 9) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     // ---------------- MMA issuer ----------------
     constexpr uint32_t kIdQK = idesc_f16(BF16, false, BM, BN);
     constexpr uint32_t kIdPV = idesc_f16(BF16, true, BM, D);
@@ -286,7 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_bar(&sb.mma_done, 0, p.status);
     }
     __syncwarp();
+  } else if (warp >= 10) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ---------------- softmax: one thread per query row ----------------
     const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + (t ? C::kS1 : C::kS0);
@@ -460,6 +480,14 @@ int launch(const Problem& p, cudaStream_t st) {
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D>::kSmem + 1024;
   auto kern = prefill_tc_kernel<D, BF16, MASK>;
+  // setmaxnreg.inc waits until the block's register pool holds the larger
+  // count, so the pool the kernel is launched with must cover the split.
+  static const bool regs_ok = [] {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, (const void*)prefill_tc_kernel<D, BF16, MASK>) != cudaSuccess) return false;
+    return a.numRegs * kThreads >= kSplitRegs;
+  }();
+  if (!regs_ok) return -1;
   cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb);
