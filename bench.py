@@ -445,6 +445,64 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+CASES = {
+    "tiny_f32_mha": lambda: wl.tiny_f32_mha(),
+    "gqa_doc_causal_bf16": lambda: wl.gqa_doc_causal_bf16(),
+    "long_causal_gqa_bf16": lambda: wl.long_causal_gqa_bf16(),
+    "decode_bnsh_bf16": lambda: wl.decode_bnsh_bf16(),
+    "cross_mask_f16": lambda: wl.cross_mask_f16(),
+    "cross_mask_f16_zero": lambda: wl.cross_mask_f16(masked_rows="zero"),
+}
+
+
+def run_case(args):
+    """Time one call of one named workload (inputs resident in HBM) and print a per-case line.
+
+    Not the benchmark line: used for the per-workload table and for profiling the
+    kernel a workload selects.  Each timed call is preceded by a 256 MiB L2 flush
+    unless --no-flush is given; the line reports the median call time."""
+    import torch
+    from attention_attn_fwd_02_gb300 import attn, build
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import GpuCase
+    build.build()
+    attn.lib()
+    torch.cuda.set_device(0)
+    case = CASES[args.case]()
+    p = case.problem
+    g = GpuCase(case, lse=True, guard=0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        g.run()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ms = []
+    for _ in range(args.steps):
+        if not args.no_flush:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g.run()
+        e1.record(st)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    rc = attn.attn_device_status()
+    med = statistics.median(ms)
+    pk, pk_kind = peaks()
+    line = {"line": "case", "case": case.name, "steps": args.steps, "warmup": args.warmup, "ms_median": med,
+            "ms_min": min(ms), "l2": "not flushed" if args.no_flush else "flushed (256 MiB write) before each call",
+            "status": attn.status_string(rc)}
+    if case.decode:
+        by = decode_kv_bytes(case)
+        line.update({"unit": "GB/s", "value": by / (med / 1e3) / 1e9, "algorithmic_bytes": by,
+                     "frac": by / (med / 1e3) / 1e9 / pk["hbm_gbs"], "peak_kind": f"{pk_kind} HBM copy"})
+    else:
+        fl = 4.0 * p["head_dim"] * wl.visible_pairs(case)
+        line.update({"unit": "TFLOP/s", "value": fl / (med / 1e3) / 1e12, "algorithmic_flops": fl,
+                     "frac": fl / (med / 1e3) / 1e12 / pk["bf16_tflops"], "peak_kind": f"{pk_kind} bf16 dense, burst"})
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,8 +516,13 @@ def main():
                     help="batch of the decode workload (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one half of the step only (for profiling); the line is then partial")
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="time one call of one named workload instead of the benchmark step (per-case line)")
+    ap.add_argument("--no-flush", action="store_true", help="with --case: keep L2 warm between calls")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.case is not None:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
