@@ -93,10 +93,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Bars sb;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Heaviest query blocks first: block L covers query block n_qblocks-1-L/(H*B).
+  // Launch order.  Causal or segmented problems: heaviest query blocks first
+  // (block L covers query block n_qblocks-1-L/(H*B)).  Otherwise every block
+  // does the same work, and the query blocks of one (batch, head) run side by
+  // side so that its K and V come from DRAM once and from L2 after that.
   const int HB = p.H * p.B;
-  const int hb = blockIdx.x % HB;
-  const int qb = n_qblocks - 1 - (int)(blockIdx.x / HB);
+  const bool lpt = p.causal || p.seg != nullptr;
+  const int hb = lpt ? (int)(blockIdx.x % HB) : (int)(blockIdx.x / n_qblocks);
+  const int qb = lpt ? n_qblocks - 1 - (int)(blockIdx.x / HB) : (int)(blockIdx.x % n_qblocks);
   const int h = hb % p.H, b = hb / p.H;
   const int g = h / p.qpg;
   const int q0 = qb * 2 * BM;
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           tmem_ld32(s_tm + c * 32, x + c * 32);
-          tmem_ld_wait();
+          tmem_ld_wait_regs<1>(x + c * 32);
 #pragma unroll
           for (int e = c * 32; e < c * 32 + 32; ++e) {
             const int kk = k0 + e;
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
-        tmem_ld_wait();
+        tmem_ld_wait_regs<BN / 32>(x);
         if (!(k0 >= lo && k0 + BN <= hi)) {
 #pragma unroll
           for (int e = 0; e < BN; ++e) {
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(o_tm + c * 32, o);
-          tmem_ld_wait();
+          tmem_ld_wait_regs<1>(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
           tmem_st32(o_tm + c * 32, o);
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(o_tm + c * 32, o);
-          tmem_ld_wait();
+          tmem_ld_wait_regs<1>(o);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;

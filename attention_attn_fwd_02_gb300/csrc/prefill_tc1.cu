@@ -72,10 +72,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Bars sb;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Heaviest query blocks first.
+  // Launch order.  Causal or segmented problems: heaviest query blocks first
+  // (block L covers query block n_qblocks-1-L/(H*B)).  Otherwise every block
+  // does the same work, and the query blocks of one (batch, head) run side by
+  // side so that its K and V come from DRAM once and from L2 after that.
   const int HB = p.H * p.B;
-  const int hb = blockIdx.x % HB;
-  const int qb = n_qblocks - 1 - (int)(blockIdx.x / HB);
+  const bool lpt = p.causal || p.seg != nullptr;
+  const int hb = lpt ? (int)(blockIdx.x % HB) : (int)(blockIdx.x / n_qblocks);
+  const int qb = lpt ? n_qblocks - 1 - (int)(blockIdx.x / HB) : (int)(blockIdx.x % n_qblocks);
   const int h = hb % p.H, b = hb / p.H;
   const int g = h / p.qpg;
   const int q0 = qb * BM;
@@ -247,6 +251,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     uint32_t x[BN];
+    // The mask slice of a key tile is loaded one tile ahead, so its latency
+    // overlaps the current tile's softmax.  A whole in-range, 16-byte-aligned
+    // slice is read with vector loads.
+    float mv[BN];
+    auto load_mask = [&](int k0) {
+      const float* mp = mrow ? mrow + k0 : nullptr;
+      if (mp && k0 + BN <= p.Sk && ((uintptr_t)mp & 15) == 0) {
+#pragma unroll
+        for (int j = 0; j < BN / 4; ++j) {
+          const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
+          mv[4 * j] = v4.x;
+          mv[4 * j + 1] = v4.y;
+          mv[4 * j + 2] = v4.z;
+          mv[4 * j + 3] = v4.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) mv[e] = (mp && k0 + e >= lo && k0 + e < hi) ? mp[e] : 0.f;
+      }
+    };
+    if (MASK && n_tiles > 0) load_mask(j0 * BN);
     for (int i = 0; i < n_tiles; ++i) {
       const int slot = i & 1;
       const uint32_t s_tm = tmem + lane_off + (slot ? C::kS1 : C::kS0);
@@ -257,28 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after();
       const int k0 = (j0 + i) * BN;
       if (explicit_x) {
-        // Scores to log2 units plus the additive mask.  A whole in-range,
-        // 16-byte-aligned mask slice is read with vector loads.
+        // Scores to log2 units plus the additive mask.
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
-        float mv[BN];
-        if (MASK) {
-          const float* mp = mrow ? mrow + k0 : nullptr;
-          if (mp && k0 + BN <= p.Sk && ((uintptr_t)mp & 15) == 0) {
-#pragma unroll
-            for (int j = 0; j < BN / 4; ++j) {
-              const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
-              mv[4 * j] = v4.x;
-              mv[4 * j + 1] = v4.y;
-              mv[4 * j + 2] = v4.z;
-              mv[4 * j + 3] = v4.w;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < BN; ++e) mv[e] = (mp && k0 + e >= lo && k0 + e < hi) ? mp[e] : 0.f;
-          }
-        }
-        tmem_ld_wait();
+        tmem_ld_wait_regs<BN / 32>(x);
 #pragma unroll
         for (int e = 0; e < BN; ++e) {
           const int kk = k0 + e;
@@ -286,10 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float v = MASK ? fmaf(s, sc, mv[e] * kLog2e) : s * sc;
           x[e] = __float_as_uint((kk >= lo && kk < hi) ? v : -INFINITY);
         }
+        if (MASK && i + 1 < n_tiles) load_mask(k0 + BN);
       } else {
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
-        tmem_ld_wait();
+        tmem_ld_wait_regs<BN / 32>(x);
         if (!(k0 >= lo && k0 + BN <= hi)) {
 #pragma unroll
           for (int e = 0; e < BN; ++e) {
@@ -344,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(o_tm + c * 32, o);
-          tmem_ld_wait();
+          tmem_ld_wait_regs<1>(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
           tmem_st32(o_tm + c * 32, o);
@@ -355,6 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sb.p_full[slot]);
     }
     // ---- epilogue: O / l, special rows, LSE ----
+    // A parity wait only tells the current phase from the one before it.
+    // S of the last tile being ready implies only that P V of the tile three
+    // back has completed (S is double-buffered, so Q K^T of tile i is issued
+    // before P V of tile i-1), so o_done may still be two phases short of the
+    // final one: wait for the second-to-last phase first, then the last.
+    if (ok && n_tiles > 1) ok = wait_warp(&sb.o_done, (uint32_t)(n_tiles - 2) & 1u, &sb.abort, p.status);
     if (ok && n_tiles > 0) ok = wait_warp(&sb.o_done, (uint32_t)(n_tiles - 1) & 1u, &sb.abort, p.status);
     if (ok) {
       fence_after();
@@ -371,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(o_tm + c * 32, o);
-          tmem_ld_wait();
+          tmem_ld_wait_regs<1>(o);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;

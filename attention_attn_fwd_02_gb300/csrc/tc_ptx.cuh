@@ -138,6 +138,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+#define ATTN_RW32(r)                                                                                                \
+  "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]),       \
+      "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),        \
+      "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),       \
+      "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+
+// A tcgen05.ld writes its registers asynchronously; they hold the loaded
+// values only after tcgen05.wait::ld.  The compiler sees the load's outputs
+// as ready at once and may schedule arithmetic on them above the wait, so
+// the wait is followed by an empty volatile statement that takes and
+// returns every loaded register: each later use then depends on it, and it
+// stays after the wait (volatile statements keep their order).
+template <int N32>
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t* r) {
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < N32; ++i) asm volatile("" : ATTN_RW32((r + 32 * i)));
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {

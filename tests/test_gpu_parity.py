@@ -84,6 +84,9 @@ EDGE = [
     ("f16", "bshd", 1, 2, 1, 127, 127, 200, False, None, False, False, "11qk", "zero", True),
     ("bf16", "bhsd", 3, 2, 2, 1, 513, 128, False, None, False, True, None, "nan", False),
     ("f32", "bhsd", 1, 2, 2, 300, 300, 256, True, None, False, False, None, "nan", False),
+    # head_dim 256 with two and three key tiles: the last P V may still be two phases behind
+    ("bf16", "bhsd", 2, 4, 2, 200, 100, 256, False, None, False, False, None, "nan", False),
+    ("f16", "bshd", 1, 3, 1, 260, 190, 256, True, None, False, True, None, "zero", False),
 ]
 
 
