@@ -1,5 +1,6 @@
 // prefill_tc1.cu -- tensor-core prefill for head_dim 256 (f16/bf16): one
-// 128-row query tile per CTA, 64-key tiles, S double-buffered in TMEM.
+// 128-row query tile per CTA, 128-key tiles, S double-buffered in TMEM, K and
+// V streamed through a ring of 32 KB shared-memory units.
 //
 // What it computes is the same as prefill_tc.cu: O = softmax(scale * Q K^T +
 // mask) V with the online normaliser of "Attention" (recursiveai.org OneGPU
@@ -12,12 +13,32 @@
 // columns, so two query tiles (the ping-pong of the head_dim <= 128 kernel)
 // do not fit the 512 columns.  Instead the overlap comes from two S buffers:
 // while the softmax warps turn S(i) into P(i), the tensor core runs P(i-1) V
-// and S(i+1) = Q K(i+1)^T.  Shared memory holds Q (64 KB) and a two-stage
-// ring of 64-key K and V tiles (32 KB each).
+// and S(i+1) = Q K(i+1)^T.
 //
-// CTA: 192 threads.  Warps 0-3: softmax, one thread per query row (= TMEM
-// lane); warp 4: TMA producer; warp 5: TMEM owner and MMA issuer.
-// TMEM: S0 [0, 64), S1 [64, 128), O [128, 128 + D).  All waits are bounded.
+// Tile sizes.  A tcgen05.mma costs its issuing thread about 48 cycles
+// whatever its size, and an M128 x N64 x K16 product runs in 32, so 64-key
+// tiles leave the tensor core waiting on issue; each tile also pays a fixed
+// few hundred cycles of barrier and TMEM round trips in the softmax.  Tiles
+// of 128 keys give N = 128 for Q K^T (64 cycles per instruction) and halve
+// the per-key fixed cost.  With S at 2 x 128 columns and O at 256, TMEM is
+// full, so Q stays in shared memory (64 KB); K and V pass through a ring of
+// four 32 KB units: a K tile is two units (head-dim halves), a V tile two
+// units (key halves), each freed as soon as the MMAs that read it complete.
+// The producer fills units in exactly the order the MMA warp consumes them:
+// K(0), K(1), then per tile i: V(i), K(i+2).
+//
+// Softmax: two threads per query row.  Warps w and w + 4 read the same 32
+// TMEM lanes (rows); warp w takes keys [0, 64) of every tile and O columns
+// [0, 128), warp w + 4 keys [64, 128) and O columns [128, 256).  The two
+// threads of a row swap their partial tile maxima through shared memory (an
+// mbarrier per warp pair, one phase per exchange), so both hold the same reference
+// maximum and make the same rescale decisions; their partial sums l are added
+// once, in the epilogue.  Two softmax warps per SM sub-partition hide each
+// other's latencies, and each thread's unrolled tile code is half as long.
+//
+// CTA: 320 threads.  Warps 0-7: softmax; warp 8: TMA producer; warp 9: TMEM
+// owner and MMA issuer.  TMEM: S0 [0, 128), S1 [128, 256), O [256, 512).
+// All waits are bounded.
 #include <string.h>
 
 #include <type_traits>
@@ -31,32 +52,75 @@ namespace tc1 {
 
 using namespace tc;
 
-constexpr int BM = 128;  // query rows per CTA
-constexpr int BN = 64;   // keys per tile
-constexpr int kThreads = 192;
+constexpr int BM = 128;                 // query rows per CTA
+constexpr int BN = 128;                 // keys per tile
+constexpr int kThreads = 320;
+constexpr int kHalf = BN / 2;           // keys per softmax thread per tile
+constexpr int kUnits = 4;               // ring units
+constexpr int kUnit = 32768;            // bytes per unit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
-constexpr float kSlack = 8.0f;  // log2 units
+constexpr float kSlack = 8.0f;          // log2 units
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t full[kUnits], empty[kUnits];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done, mma_done;
+  uint64_t pair[4];          // per softmax warp pair (w, w + 4): one phase per exchange
   uint32_t tmem_base;
   int abort;
   int lo_u, hi_u;
+  float red_max[2][2][BM];   // [tile parity][key half][row]: partial tile maxima
+  float red_l[2][BM];        // [key half][row]: partial sums for the epilogue
 };
 
 template <int D>
 struct Cfg {
-  static constexpr int kChunks = D / 64;
-  static constexpr int kStages = 2;
-  static constexpr int kQTile = BM * D * 2;
-  static constexpr int kKTile = BN * D * 2;
-  static constexpr int kSmem = kQTile + 2 * kStages * kKTile;
+  static_assert(D == 256, "this kernel is laid out for head_dim 256");
+  static constexpr int kQTile = BM * D * 2;                      // 64 KB
+  static constexpr int kSmem = kQTile + kUnits * kUnit;          // 192 KB
   static constexpr int kS0 = 0, kS1 = BN, kO = 2 * BN;
-  static_assert(2 * BN + D <= 512, "TMEM budget");
+  static_assert(kO + D <= 512, "TMEM budget");
+  // A K unit holds one head-dim half of a key tile: 2 chunks of [128 keys][128 B].
+  // A V unit holds one key half of a value tile: 4 chunks of [64 keys][128 B].
+  static_assert(2 * BN * 128 == kUnit && 4 * (BN / 2) * 128 == kUnit, "unit layout");
+};
+
+// Unit sequence shared by the producer and the MMA warp: K(0), K(1), then for
+// every tile i: V(i), and K(i+2) when it exists.  Each K or V tile is two units.
+struct UnitSeq {
+  int n_tiles, step = 0;
+  // Returns false at the end; otherwise (kind, tile, half): kind 0 = K, 1 = V.
+  __device__ bool next(int& kind, int& tile, int& half) {
+    const int pre = n_tiles >= 2 ? 4 : 2 * n_tiles;  // prologue units
+    if (step < pre) {
+      kind = 0;
+      tile = step / 2;
+      half = step % 2;
+    } else {
+      // after the prologue: groups of V(i) (2 units) and K(i+2) (2 units if i+2 < n)
+      int s = step - pre, i = 0;
+      // units per tile i: 2 + (i + 2 < n_tiles ? 2 : 0); the first n_tiles-2 tiles have 4
+      const int full_groups = n_tiles > 2 ? n_tiles - 2 : 0;
+      if (s < 4 * full_groups) {
+        i = s / 4;
+        const int r = s % 4;
+        kind = r < 2 ? 1 : 0;
+        tile = r < 2 ? i : i + 2;
+        half = r % 2;
+      } else {
+        s -= 4 * full_groups;
+        i = full_groups + s / 2;
+        if (i >= n_tiles) return false;
+        kind = 1;
+        tile = i;
+        half = s % 2;
+      }
+    }
+    ++step;
+    return true;
+  }
 };
 
 template <int D, bool BF16, bool MASK>
@@ -67,8 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;
-  uint8_t* k_s = q_s + C::kQTile;
-  uint8_t* v_s = k_s + C::kStages * C::kKTile;
+  uint8_t* ring = q_s + C::kQTile;
   __shared__ Bars sb;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -84,10 +147,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = h / p.qpg;
   const int q0 = qb * BM;
 
-  const int r = warp * 32 + lane;  // softmax row = TMEM lane (warps 0-3)
+  const int r = (warp % 4) * 32 + lane;  // softmax row = TMEM lane (warps 0-7)
+  const int ch = warp / 4;                // key half / O half of a softmax thread
   const int qrow = q0 + r;
   int lo = 0, hi = 0;
-  if (warp < 4 && qrow < p.Sq) {
+  if (warp < 8 && qrow < p.Sq) {
     int64_t lo64, hi64;
     row_range(p, b, qrow, lo64, hi64);
     lo = (int)lo64;
@@ -98,21 +162,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     sb.hi_u = -1;
     sb.abort = 0;
     mbar_init(&sb.q_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&sb.k_full[s], 1);
-      mbar_init(&sb.k_empty[s], 1);
-      mbar_init(&sb.v_full[s], 1);
-      mbar_init(&sb.v_empty[s], 1);
+    for (int u = 0; u < kUnits; ++u) {
+      mbar_init(&sb.full[u], 1);
+      mbar_init(&sb.empty[u], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.s_full[i], 1);
-      mbar_init(&sb.p_full[i], BM);
+      mbar_init(&sb.p_full[i], 2 * BM);
     }
     mbar_init(&sb.o_done, 1);
     mbar_init(&sb.mma_done, 1);
+    for (int w = 0; w < 4; ++w) mbar_init(&sb.pair[w], 64);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&sb.tmem_base))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -120,7 +183,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp < 4 && hi > lo) {
+  // Q does not depend on the key range: its copy starts at once.
+  if (threadIdx.x == 8 * 32) {
+    mbar_expect_tx(&sb.q_full, C::kQTile);
+    for (int c = 0; c < D / 64; ++c) tma_load_4d(q_s + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0, h, b);
+  }
+  if (warp < 4 && hi > lo) {   // the rows' ranges (warps 4-7 hold the same rows)
     atomicMin(&sb.lo_u, lo);
     atomicMax(&sb.hi_u, hi);
   }
@@ -131,117 +199,142 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j0 = any ? lo_u / BN : 0;
   const int n_tiles = any ? (hi_u + BN - 1) / BN - j0 : 0;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
-    if (lane == 0 && n_tiles > 0) {
-      int issued = 0, k_only = -1;
-      mbar_expect_tx(&sb.q_full, C::kQTile);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d(q_s + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0, h, b);
-      for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % C::kStages;
-        const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-        const int krow = (j0 + i) * BN;
-        if (!wait_bar(&sb.k_empty[s], ph ^ 1u, &sb.abort, p.status)) break;
-        mbar_expect_tx(&sb.k_full[s], C::kKTile);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(k_s + s * C::kKTile + c * BN * 128, &tm_k, &sb.k_full[s], c * 64, krow, g, b);
-        if (!wait_bar(&sb.v_empty[s], ph ^ 1u, &sb.abort, p.status)) {
-          k_only = i;
-          break;
+    if (lane == 0) {
+      UnitSeq seq{n_tiles};
+      int kind, tile, half, issued = 0;
+      while (seq.next(kind, tile, half)) {
+        const int u = issued % kUnits;
+        const uint32_t ph = (uint32_t)(issued / kUnits) & 1u;
+        if (!wait_bar(&sb.empty[u], ph ^ 1u, &sb.abort, p.status)) break;
+        mbar_expect_tx(&sb.full[u], kUnit);
+        uint8_t* dst = ring + u * kUnit;
+        const int krow = (j0 + tile) * BN;
+        if (kind == 0) {
+          // head-dim half `half` of K rows [krow, krow + 128): two 64-column chunks
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(dst + c * BN * 128, &tm_k, &sb.full[u], (2 * half + c) * 64, krow, g, b);
+        } else {
+          // key half `half` of V rows: four 64-column chunks of 64 rows
+          for (int c = 0; c < 4; ++c)
+            tma_load_4d(dst + c * (BN / 2) * 128, &tm_v, &sb.full[u], c * 64, krow + half * (BN / 2), g, b);
         }
-        mbar_expect_tx(&sb.v_full[s], C::kKTile);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(v_s + s * C::kKTile + c * BN * 128, &tm_v, &sb.v_full[s], c * 64, krow, g, b);
-        issued = i + 1;
+        ++issued;
       }
-      // Copies still in flight land before the CTA can exit.
+      // Copies still in flight land before the CTA can exit: the last kUnits
+      // units issued are the only ones not known to have been consumed.
       drain_bar(&sb.q_full, 0, p.status);
-      for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i) {
-        drain_bar(&sb.k_full[i % C::kStages], (uint32_t)(i / C::kStages) & 1u, p.status);
-        drain_bar(&sb.v_full[i % C::kStages], (uint32_t)(i / C::kStages) & 1u, p.status);
-      }
-      if (k_only >= 0)
-        drain_bar(&sb.k_full[k_only % C::kStages], (uint32_t)(k_only / C::kStages) & 1u, p.status);
+      for (int j = issued > kUnits ? issued - kUnits : 0; j < issued; ++j)
+        drain_bar(&sb.full[j % kUnits], (uint32_t)(j / kUnits) & 1u, p.status);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t kIdQK = idesc_f16(BF16, false, BM, BN);
     constexpr uint32_t kIdPV = idesc_f16(BF16, true, BM, D);
-    const uint32_t q_addr = su32(q_s), k_addr = su32(k_s), v_addr = su32(v_s);
-    auto issue_qk = [&](int slot, int s) {  // S[slot] = Q K(stage s)^T
-      fence_after();
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t a = sdesc(q_addr + (uint32_t)((kk / 4) * BM * 128 + (kk % 4) * 32), 16, 1024);
-        const uint64_t bd = sdesc(k_addr + s * C::kKTile + (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32), 16, 1024);
-        mma_ss(tmem + (slot ? C::kS1 : C::kS0), a, bd, kIdQK, kk > 0);
-      }
-    };
-    auto issue_pv = [&](int slot, int s, bool first) {  // O += P[slot] V(stage s)
-      fence_after();
-#pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t bd = sdesc(v_addr + s * C::kKTile + kk * 16 * 128, BN * 128, 1024);
-        mma_ts(tmem + C::kO, tmem + (slot ? C::kS1 : C::kS0) + kk * 8, bd, kIdPV, (!first || kk > 0) ? 1u : 0u);
-      }
-    };
+    const uint32_t q_addr = su32(q_s), ring_addr = su32(ring);
+    int taken = 0;  // units consumed so far (ring position)
     bool ok = n_tiles > 0;
-    if (ok) ok = wait_warp(&sb.q_full, 0, &sb.abort, p.status);
-    // Prologue: S of the first two key tiles.
-    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-      if (!(ok = wait_warp(&sb.k_full[j], 0, &sb.abort, p.status))) break;
-      if (lane == 0) {
-        issue_qk(j, j);
-        mma_commit(&sb.s_full[j]);
-        mma_commit(&sb.k_empty[j]);
-      }
-      __syncwarp();
-    }
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      const int s = i % C::kStages;  // stage and S slot coincide
-      const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-      const int k0 = (j0 + i) * BN;
-      if (!wait_warp(&sb.v_full[s], ph, &sb.abort, p.status)) break;
-      // Zero the V rows of keys no row of this CTA sees (they may hold anything).
-      if (k0 < lo_u || k0 + BN > hi_u) {
-        for (int u = lane; u < BN * C::kChunks * 8; u += 32) {
-          const int row = u / (C::kChunks * 8);
-          const int rest = u % (C::kChunks * 8);
-          const int kk = k0 + row;
-          if (kk < lo_u || kk >= hi_u)
-            *reinterpret_cast<uint4*>(v_s + s * C::kKTile + (rest / 8) * BN * 128 + row * 128 + (rest % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      __syncwarp();
-      if (!wait_warp(&sb.p_full[s], ph, &sb.abort, p.status)) break;
-      if (lane == 0) {
-        issue_pv(s, s, i == 0);
-        mma_commit(&sb.o_done);
-        mma_commit(&sb.v_empty[s]);
-      }
-      __syncwarp();
-      if (i + 2 < n_tiles) {
-        if (!wait_warp(&sb.k_full[s], (uint32_t)((i + 2) / C::kStages) & 1u, &sb.abort, p.status)) break;
+    // Waits for the next unit; returns its shared address (0 on abort).
+    auto take = [&]() -> uint32_t {
+      const int u = taken % kUnits;
+      const uint32_t ph = (uint32_t)(taken / kUnits) & 1u;
+      ++taken;
+      if (!wait_warp(&sb.full[u], ph, &sb.abort, p.status)) return 0u;
+      return ring_addr + (uint32_t)(u * kUnit);
+    };
+    // The unit just taken is released when the MMAs issued so far complete.
+    auto give = [&]() {
+      if (lane == 0) mma_commit(&sb.empty[(taken - 1) % kUnits]);
+    };
+    // S[slot] = Q K(tile)^T: 16 MMAs of K = 16, the first 8 from the low
+    // head-dim half of K, the rest from the high half.
+    auto issue_qk = [&](int slot) -> bool {
+      for (int hf = 0; hf < 2; ++hf) {
+        const uint32_t ku = take();
+        if (!ku) return false;
         if (lane == 0) {
-          issue_qk(s, s);
-          mma_commit(&sb.s_full[s]);
-          mma_commit(&sb.k_empty[s]);
+          fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int kq = hf * 8 + kk;  // K-step over head_dim
+            const uint64_t a = sdesc(q_addr + (uint32_t)((kq / 4) * BM * 128 + (kq % 4) * 32), 16, 1024);
+            const uint64_t bd = sdesc(ku + (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32), 16, 1024);
+            mma_ss(tmem + (slot ? C::kS1 : C::kS0), a, bd, kIdQK, kq > 0);
+          }
         }
         __syncwarp();
+        give();
       }
+      if (lane == 0) mma_commit(&sb.s_full[slot]);
+      __syncwarp();
+      return true;
+    };
+    // O += P[slot] V(tile): 8 MMAs of K = 16 keys, 4 per V unit.
+    auto issue_pv = [&](int slot, int tile, bool first) -> bool {
+      const int k0 = (j0 + tile) * BN;
+      for (int hf = 0; hf < 2; ++hf) {
+        const uint32_t vu = take();
+        if (!vu) return false;
+        const int kb = k0 + hf * (BN / 2);
+        // Zero the V rows of keys no row of this CTA sees (they may hold anything).
+        if (kb < lo_u || kb + BN / 2 > hi_u) {
+          uint8_t* vp = ring + (vu - ring_addr);
+          for (int w = lane; w < (BN / 2) * 4 * 8; w += 32) {
+            const int row = w / 32, rest = w % 32;   // 4 chunks x 8 16-byte pieces per row
+            const int kk = kb + row;
+            if (kk < lo_u || kk >= hi_u)
+              *reinterpret_cast<uint4*>(vp + (rest / 8) * (BN / 2) * 128 + row * 128 + (rest % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) {
+          fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = sdesc(vu + (uint32_t)(kk * 16 * 128), (BN / 2) * 128, 1024);
+            mma_ts(tmem + C::kO, tmem + (slot ? C::kS1 : C::kS0) + (hf * 4 + kk) * 8, bd, kIdPV,
+                   (!first || hf > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+        give();
+      }
+      if (lane == 0) mma_commit(&sb.o_done);
+      __syncwarp();
+      return true;
+    };
+    if (ok) ok = wait_warp(&sb.q_full, 0, &sb.abort, p.status);
+    // Prologue: S of the first two key tiles.
+    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_qk(j);
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int slot = i & 1;
+      if (!(ok = wait_warp(&sb.p_full[slot], (uint32_t)(i >> 1) & 1u, &sb.abort, p.status))) break;
+      if (!(ok = issue_pv(slot, i, i == 0))) break;
+      // Q K^T of tile i+2 into the S buffer P(i) just left (the tensor core
+      // runs a thread's MMAs in issue order, so P V(i) reads P first).
+      if (i + 2 < n_tiles && !(ok = issue_qk(slot))) break;
     }
-    if (lane == 0 && n_tiles > 0) {
+    // Every MMA issued above has completed before TMEM is freed.
+    if (lane == 0 && taken > 0) {
       mma_commit(&sb.mma_done);
       drain_bar(&sb.mma_done, 0, p.status);
     }
     __syncwarp();
   } else {
-    // ---------------- softmax: one thread per query row ----------------
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t o_tm = tmem + lane_off + C::kO;
+    // ---------------- softmax: two threads per query row ----------------
+    const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t o_tm = tmem + lane_off + C::kO + ch * (D / 2);
+    // Exchange point of warps w and w + 4: both arrive, then wait (bounded)
+    // for the phase; the arrive releases and the wait acquires the shared
+    // memory written before it.
+    uint64_t* pair_bar = &sb.pair[warp % 4];
+    auto pair_sync = [&](int phase) -> bool {
+      mbar_arrive(pair_bar);
+      return wait_warp(pair_bar, (uint32_t)phase & 1u, &sb.abort, p.status);
+    };
     const float sc = p.scale * kLog2e;
     const bool explicit_x = MASK || !(sc > 0.f);
     const float c_eff = explicit_x ? 1.f : sc;
@@ -250,69 +343,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       mrow = p.M + p.m.off + (int64_t)b * p.m.bs + (int64_t)h * p.m.hs + (int64_t)qrow * p.m.rs;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    uint32_t x[BN];
-    // The mask slice of a key tile is loaded one tile ahead, so its latency
-    // overlaps the current tile's softmax.  A whole in-range, 16-byte-aligned
-    // slice is read with vector loads.
-    float mv[BN];
-    auto load_mask = [&](int k0) {
-      const float* mp = mrow ? mrow + k0 : nullptr;
-      if (mp && k0 + BN <= p.Sk && ((uintptr_t)mp & 15) == 0) {
-#pragma unroll
-        for (int j = 0; j < BN / 4; ++j) {
-          const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
-          mv[4 * j] = v4.x;
-          mv[4 * j + 1] = v4.y;
-          mv[4 * j + 2] = v4.z;
-          mv[4 * j + 3] = v4.w;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) mv[e] = (mp && k0 + e >= lo && k0 + e < hi) ? mp[e] : 0.f;
-      }
-    };
-    if (MASK && n_tiles > 0) load_mask(j0 * BN);
+    uint32_t x[kHalf];
     for (int i = 0; i < n_tiles; ++i) {
       const int slot = i & 1;
       const uint32_t s_tm = tmem + lane_off + (slot ? C::kS1 : C::kS0);
+      const int k0 = (j0 + i) * BN + ch * kHalf;   // this thread's first key
+      float mv[kHalf];
+      if (MASK) {
+        // Mask values of this thread's 64 keys (vector loads when the slice is
+        // in range and 16-byte aligned; hidden keys read as 0).  Issued before
+        // the wait for S so their latency overlaps it.
+        const float* mp = mrow ? mrow + k0 : nullptr;
+        if (mp && k0 + kHalf <= p.Sk && ((uintptr_t)mp & 15) == 0) {
+#pragma unroll
+          for (int j = 0; j < kHalf / 4; ++j) {
+            const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
+            mv[4 * j] = v4.x;
+            mv[4 * j + 1] = v4.y;
+            mv[4 * j + 2] = v4.z;
+            mv[4 * j + 3] = v4.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) mv[e] = (mp && k0 + e >= lo && k0 + e < hi) ? mp[e] : 0.f;
+        }
+      }
       if (!wait_warp(&sb.s_full[slot], (uint32_t)(i >> 1) & 1u, &sb.abort, p.status)) {
         ok = false;
         break;
       }
       fence_after();
-      const int k0 = (j0 + i) * BN;
+      tmem_ld32(s_tm + ch * kHalf, x);
+      tmem_ld32(s_tm + ch * kHalf + 32, x + 32);
+      tmem_ld_wait_regs<2>(x);
       if (explicit_x) {
         // Scores to log2 units plus the additive mask.
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
-        tmem_ld_wait_regs<BN / 32>(x);
-#pragma unroll
-        for (int e = 0; e < BN; ++e) {
+        for (int e = 0; e < kHalf; ++e) {
           const int kk = k0 + e;
           const float s = __uint_as_float(x[e]);
           const float v = MASK ? fmaf(s, sc, mv[e] * kLog2e) : s * sc;
           x[e] = __float_as_uint((kk >= lo && kk < hi) ? v : -INFINITY);
         }
-        if (MASK && i + 1 < n_tiles) load_mask(k0 + BN);
-      } else {
+      } else if (!(k0 >= lo && k0 + kHalf <= hi)) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
-        tmem_ld_wait_regs<BN / 32>(x);
-        if (!(k0 >= lo && k0 + BN <= hi)) {
-#pragma unroll
-          for (int e = 0; e < BN; ++e) {
-            const int kk = k0 + e;
-            if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
-          }
+        for (int e = 0; e < kHalf; ++e) {
+          const int kk = k0 + e;
+          if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
         }
       }
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < BN; e += 4) {
+      for (int e = 0; e < kHalf; e += 4) {
         mx0 = max3(mx0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
         mx1 = max3(mx1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
       }
-      const float mt = fmaxf(mx0, mx1) * c_eff;
+      // Swap partial maxima with the other thread of this row.  The barrier
+      // also orders both threads' loads of S before either stores P over it
+      // (P of keys 64..127 lands on columns that held S of keys 32..63).
+      sb.red_max[slot][ch][r] = fmaxf(mx0, mx1);
+      fence_before();
+      if (!pair_sync(i)) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      const float mt = fmaxf(sb.red_max[slot][0][r], sb.red_max[slot][1][r]) * c_eff;
       const bool raise = mt > m_ref + kSlack;  // also true for the first tile with a visible key
       float corr = 1.f;
       if (raise) corr = ex2(m_ref - mt);       // 0 when m_ref = -inf
@@ -325,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t c2 = f2u(c_eff, c_eff), n2 = f2u(neg, neg);
       float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < BN; e += 4) {
+      for (int e = 0; e < kHalf; e += 4) {
         float a0, a1, b0, b1;
         fma2(a0, a1, __uint_as_float(x[e]), __uint_as_float(x[e + 1]), c2, n2);
         fma2(b0, b1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]), c2, n2);
@@ -339,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         x[e / 2 + 1] = pack2<BF16>(b0, b1);
       }
       l += (la0 + la1) + (lb0 + lb1);
-      tmem_st32(s_tm, x);  // P of the 64 keys: 32 packed columns
+      tmem_st32(s_tm + ch * (kHalf / 2), x);  // P of this thread's 64 keys: 32 packed columns
       if (__any_sync(0xffffffffu, rescale)) {
         // P V of the previous tile must have landed in O before it is scaled.
         if (!wait_warp(&sb.o_done, (uint32_t)(i - 1) & 1u, &sb.abort, p.status)) {
@@ -349,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after();
         const float f = rescale ? corr : 1.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t o[32];
           tmem_ld32(o_tm + c * 32, o);
           tmem_ld_wait_regs<1>(o);
@@ -370,18 +466,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // final one: wait for the second-to-last phase first, then the last.
     if (ok && n_tiles > 1) ok = wait_warp(&sb.o_done, (uint32_t)(n_tiles - 2) & 1u, &sb.abort, p.status);
     if (ok && n_tiles > 0) ok = wait_warp(&sb.o_done, (uint32_t)(n_tiles - 1) & 1u, &sb.abort, p.status);
+    // The row's sum is the two threads' partial sums (same reference maximum).
+    sb.red_l[ch][r] = l;
+    if (ok) ok = pair_sync(n_tiles);
+    l = sb.red_l[0][r] + sb.red_l[1][r];
     if (ok) {
       fence_after();
       const bool valid = qrow < p.Sq;
       const bool hidden_row = (l == 0.f);  // no visible key; a NaN l stays a NaN row
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* orow = valid ? static_cast<T*>(p.O) + p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs +
-                            (int64_t)qrow * p.o.rs
+                            (int64_t)qrow * p.o.rs + ch * (D / 2)
                       : nullptr;
       const float inv = 1.f / l;
       const float fill = p.masked_zero ? 0.f : NAN;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(o_tm + c * 32, o);
@@ -403,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
         }
       }
-      if (valid && p.lse)
+      if (valid && p.lse && ch == 0)
         p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
             hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
     }
@@ -411,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
   }
@@ -422,7 +522,7 @@ int launch(const Problem& p, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!tma_map_bhsd(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q, BM) ||
       !tma_map_bhsd(&mk, p.K, p.dtype, D, p.Sk, p.G, p.B, p.k, BN) ||
-      !tma_map_bhsd(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v, BN))
+      !tma_map_bhsd(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v, BN / 2))
     return -1;  // not describable: caller falls back
   const int nqb = (p.Sq + BM - 1) / BM;
   const int64_t blocks = (int64_t)nqb * p.H * p.B;
