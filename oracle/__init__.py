@@ -59,7 +59,8 @@ class _Problem(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("causal", ctypes.c_int32),
                 ("causal_offset", ctypes.c_int64), ("masked_rows_zero", ctypes.c_int32),
                 ("q", _Layout), ("k", _Layout), ("v", _Layout), ("mask", _Layout),
-                ("seg_batch_stride", ctypes.c_int64)]
+                ("seg_batch_stride", ctypes.c_int64), ("window_left", ctypes.c_int32),
+                ("causal_align", ctypes.c_int32), ("k_lens_kind", ctypes.c_int32)]
 
 
 def _load():
@@ -106,7 +107,8 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
       ('f32'|'f16'|'bf16'), scale (0 = default), causal, causal_offset (None =
       k_len - q_len), masked_rows ('nan'|'zero'), q_layout/k_layout/v_layout
       and mask_layout as (offset, batch_stride, head_stride, row_stride) in
-      elements, seg_batch_stride.
+      elements, seg_batch_stride; optional window_left (None/-1 = off),
+      causal_align ('fixed' | 'klens'), k_lens_kind ('count' | 'last_index').
     q, k, v: raw storage (float32 for f32, uint16 bit patterns for f16/bf16),
       indexed through the layouts.  mask: float32 storage; seg, k_lens: int32.
     rows: None for every (b, h, qi) row in that order, else an int array [n, 3].
@@ -133,6 +135,10 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
     prob.v = _Layout(*p["v_layout"])
     prob.mask = _Layout(*(p.get("mask_layout") or (0, 0, 0, 0)))
     prob.seg_batch_stride = int(p.get("seg_batch_stride", p["q_len"]))
+    w = p.get("window_left")
+    prob.window_left = -1 if w is None else int(w)
+    prob.causal_align = 1 if p.get("causal_align") in ("klens", 1) else 0
+    prob.k_lens_kind = 1 if p.get("k_lens_kind") in ("last_index", 1) else 0
     if rows is None:
         n_rows = p["batch"] * p["heads"] * p["q_len"]
         rows_arr = None

@@ -32,7 +32,19 @@
  *   - a row with a NaN or +inf score among its visible keys gives NaN in
  *     every output element and NaN LSE, in both masked-rows modes;
  *   - the default causal offset is k_len - q_len; the default scale is the
- *     float32 value nearest 1/sqrt(head_dim).
+ *     float32 value nearest 1/sqrt(head_dim);
+ *   - local (sliding-window) attention with left window w keeps, for a causal
+ *     row whose diagonal key is i + offset, the keys i + offset - w .. i +
+ *     offset (w + 1 keys at most; w = 0 keeps the diagonal key alone);
+ *   - the right-aligned causal bound of chunked prefill uses, for batch entry
+ *     b, the offset (clamped key length of b) - q_len in place of the single
+ *     offset;
+ *   - key lengths given as "last index" (ONNX seqlens_k) are counts minus one.
+ *
+ * The three visibility variants follow "com.microsoft.GroupQueryAttention"
+ * (webgpu-kernels README): attribute local_window_size, input seqlens_k, and
+ * its chunked-prefill variants, whose causal bound is right-aligned to each
+ * sample's live length.
  *
  * Precision: every product and sum is in double.  Inputs are read in their
  * storage type (float32, IEEE half or bfloat16 bit patterns) and widened
@@ -63,6 +75,9 @@ typedef struct {
   orc_layout q, k, v;
   orc_layout mask;        /* (batch, head, row) strides in floats; keys contiguous */
   int64_t seg_batch_stride;
+  int32_t window_left;    /* -1: no window; else causal rows keep keys >= i + offset - window_left */
+  int32_t causal_align;   /* 0: one offset; 1: batch b's offset is its clamped key length - q_len */
+  int32_t k_lens_kind;    /* 0: k_lens are counts; 1: they are the last valid index (count - 1) */
 } orc_problem;
 
 /* ---- exact widening of the storage types --------------------------------- */
@@ -136,13 +151,17 @@ typedef struct {
  * "attention_forward ...", section "2) Phase 0". */
 static int orc_visible(const orc_problem* p, const int32_t* seg, const int32_t* k_lens,
                        int64_t b, int64_t qi, int64_t kk) {
+  int64_t kl = p->k_len;                        /* valid keys of this batch entry */
   if (k_lens) {
-    int64_t kl = orc_clamp((int64_t)k_lens[b], 0, p->k_len);
+    kl = orc_clamp((int64_t)k_lens[b] + (p->k_lens_kind ? 1 : 0), 0, p->k_len);
     if (kk >= kl) return 0;
   }
   if (p->causal) {
-    int64_t off = p->causal_offset == INT64_MIN ? (int64_t)p->k_len - p->q_len : p->causal_offset;
-    if (kk > qi + off) return 0;
+    int64_t off;
+    if (p->causal_align) off = kl - p->q_len;  /* right-aligned to this entry's live length */
+    else off = p->causal_offset == INT64_MIN ? (int64_t)p->k_len - p->q_len : p->causal_offset;
+    if (kk > qi + off) return 0;                /* after the row's diagonal key */
+    if (p->window_left >= 0 && kk < qi + off - p->window_left) return 0;   /* left of the window */
   }
   if (seg) {
     int64_t start = orc_clamp((int64_t)seg[b * p->seg_batch_stride + qi], 0, p->k_len);
