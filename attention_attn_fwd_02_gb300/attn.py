@@ -20,6 +20,8 @@ ATTN_MASKED_ROWS_NAN, ATTN_MASKED_ROWS_ZERO = 0, 1
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_ALIGNMENT = 0, 1, 2, 3
 ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = 4, 5, 6
 ATTN_OFFSET_DEFAULT = -(2**63)
+ATTN_CAUSAL_FIXED, ATTN_CAUSAL_KLENS = 0, 1
+ATTN_KLENS_COUNT, ATTN_KLENS_LAST_INDEX = 0, 1
 DTYPE_CODE = {"f32": ATTN_F32, "f16": ATTN_F16, "bf16": ATTN_BF16}
 EXPORTS = ("attn_fwd_workspace_size", "attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_combine",
            "attn_device_status", "attn_status_string", "attn_version", "attn_decode_noalloc",
@@ -38,7 +40,9 @@ class attn_problem(ctypes.Structure):
                 ("causal_offset", ctypes.c_int64), ("masked_rows", ctypes.c_int32),
                 ("q", attn_layout), ("k", attn_layout), ("v", attn_layout), ("o", attn_layout),
                 ("mask", attn_layout), ("seg_batch_stride", ctypes.c_int64),
-                ("lse_batch_stride", ctypes.c_int64), ("lse_head_stride", ctypes.c_int64)]
+                ("lse_batch_stride", ctypes.c_int64), ("lse_head_stride", ctypes.c_int64),
+                ("window_left", ctypes.c_int32), ("causal_align", ctypes.c_int32),
+                ("k_lens_kind", ctypes.c_int32)]
 
 
 class AttnError(RuntimeError):
@@ -150,6 +154,11 @@ def make_problem(d: dict) -> attn_problem:
     p.seg_batch_stride = int(d.get("seg_batch_stride", d["q_len"]))
     lb, lh = d.get("lse_layout") or (d["heads"] * d["q_len"], d["q_len"])
     p.lse_batch_stride, p.lse_head_stride = lb, lh
+    w = d.get("window_left")
+    p.window_left = -1 if w is None else int(w)
+    p.causal_align = ATTN_CAUSAL_KLENS if d.get("causal_align") in ("klens", ATTN_CAUSAL_KLENS) else ATTN_CAUSAL_FIXED
+    p.k_lens_kind = (ATTN_KLENS_LAST_INDEX if d.get("k_lens_kind") in ("last_index", ATTN_KLENS_LAST_INDEX)
+                     else ATTN_KLENS_COUNT)
     return p
 
 
@@ -183,10 +192,14 @@ def _check(code, where):
 
 
 def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, mask=None, seg=None,
-        k_lens=None, masked_rows="nan", return_lse=False, out=None, lse=None, stream=None):
+        k_lens=None, masked_rows="nan", return_lse=False, out=None, lse=None, stream=None,
+        window_left=None, causal_align="fixed", k_lens_kind="count"):
     """O (and LSE) for torch CUDA tensors.  layout 'bshd': Q [B,Sq,H,D], K/V [B,Sk,G,D];
     'bhsd': Q [B,H,Sq,D], K/V [B,G,Sk,D].  mask: float32 broadcastable 4-D [B|1, H|1, Sq|1, Sk]
-    with contiguous keys; seg: int32 [B, Sq] or [Sq]; k_lens: int32 [B]."""
+    with contiguous keys; seg: int32 [B, Sq] or [Sq]; k_lens: int32 [B].  window_left: left
+    window of causal local attention (None = off); causal_align: 'fixed' (one offset) or
+    'klens' (each entry's diagonal right-aligned to its key length); k_lens_kind: 'count' or
+    'last_index' (ONNX seqlens_k, count minus one)."""
     torch = _torch()
     hd = 2 if layout == "bshd" else 1
     sd = 1 if layout == "bshd" else 2
@@ -197,7 +210,8 @@ def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, 
     d = dict(batch=B, heads=H, kv_heads=G, q_len=Sq, k_len=Sk, head_dim=D, dtype=_dtype_name(q), scale=scale,
              causal=causal, causal_offset=causal_offset, masked_rows=masked_rows,
              q_layout=_layout4(q, hd), k_layout=_layout4(k, hd), v_layout=_layout4(v, hd),
-             o_layout=_layout4(out, hd))
+             o_layout=_layout4(out, hd), window_left=window_left, causal_align=causal_align,
+             k_lens_kind=k_lens_kind)
     if mask is not None:
         if mask.dtype != torch.float32 or mask.dim() != 4 or mask.stride(3) != 1:
             raise ValueError("mask must be float32, 4-D, keys contiguous")
@@ -219,16 +233,19 @@ def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, 
 
 
 def decode(q, k_cache, v_cache, k_lens=None, *, scale=0.0, mask=None, masked_rows="nan", return_lse=False,
-           out=None, lse=None, workspace=None, stream=None):
-    """Single-query decode: q [B, 1, H, D]; caches BNSH [B, G, cap, D]; k_lens int32 [B]."""
+           out=None, lse=None, workspace=None, stream=None, window_left=None, k_lens_kind="count"):
+    """Single-query decode: q [B, 1, H, D]; caches BNSH [B, G, cap, D]; k_lens int32 [B].
+    window_left keeps only the last window_left + 1 valid keys (local attention);
+    k_lens_kind 'last_index' takes ONNX seqlens_k (count minus one) as given."""
     torch = _torch()
     B, Sq, H, D = q.shape
     G, cap = k_cache.shape[1], k_cache.shape[2]
     if out is None:
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     d = dict(batch=B, heads=H, kv_heads=G, q_len=Sq, k_len=cap, head_dim=D, dtype=_dtype_name(q), scale=scale,
-             causal=False, masked_rows=masked_rows, q_layout=_layout4(q, 2), k_layout=_layout4(k_cache, 1),
-             v_layout=_layout4(v_cache, 1), o_layout=_layout4(out, 2))
+             causal=window_left is not None, causal_align="klens", window_left=window_left,
+             k_lens_kind=k_lens_kind, masked_rows=masked_rows, q_layout=_layout4(q, 2),
+             k_layout=_layout4(k_cache, 1), v_layout=_layout4(v_cache, 1), o_layout=_layout4(out, 2))
     if mask is not None:
         d["mask_layout"] = (0, mask.stride(0) if mask.shape[0] > 1 else 0,
                             mask.stride(1) if mask.shape[1] > 1 else 0, mask.stride(2) if mask.shape[2] > 1 else 0)

@@ -60,6 +60,9 @@ int check_problem(const attn_problem* p) {
   if (!layout_ok(p->q) || !layout_ok(p->k) || !layout_ok(p->v) || !layout_ok(p->o) || !layout_ok(p->mask))
     return ATTN_ERR_INVALID_ARG;
   if (p->seg_batch_stride < 0 || p->lse_batch_stride < 0 || p->lse_head_stride < 0) return ATTN_ERR_INVALID_ARG;
+  if (p->window_left < -1 || (p->window_left >= 0 && !p->causal)) return ATTN_ERR_INVALID_ARG;
+  if (p->causal_align != ATTN_CAUSAL_FIXED && p->causal_align != ATTN_CAUSAL_KLENS) return ATTN_ERR_INVALID_ARG;
+  if (p->k_lens_kind != ATTN_KLENS_COUNT && p->k_lens_kind != ATTN_KLENS_LAST_INDEX) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -79,6 +82,9 @@ Problem resolve(const attn_problem* p, const void* q, const void* k, const void*
   r.causal = p->causal;
   r.coff = p->causal_offset == ATTN_OFFSET_DEFAULT ? (int64_t)p->k_len - p->q_len : p->causal_offset;
   r.masked_zero = p->masked_rows == ATTN_MASKED_ROWS_ZERO;
+  r.window = p->window_left;
+  r.align_klens = p->causal_align == ATTN_CAUSAL_KLENS;
+  r.klens_plus = p->k_lens_kind == ATTN_KLENS_LAST_INDEX ? 1 : 0;
   r.q = {p->q.offset, p->q.batch_stride, p->q.head_stride, p->q.row_stride};
   r.k = {p->k.offset, p->k.batch_stride, p->k.head_stride, p->k.row_stride};
   r.v = {p->v.offset, p->v.batch_stride, p->v.head_stride, p->v.row_stride};
@@ -252,6 +258,6 @@ const char* attn_status_string(int status) {
   }
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 200; }
 
 }  // extern "C"

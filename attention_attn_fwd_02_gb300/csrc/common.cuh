@@ -24,6 +24,9 @@ struct Problem {
   int causal;
   int64_t coff;                  // causal offset (resolved)
   int masked_zero;
+  int window;                    // left window (keys behind the diagonal), -1 = none
+  int align_klens;               // 1: causal offset of entry b is L_b - Sq
+  int klens_plus;                // added to k_lens[b] (1 for last-index lengths)
   Layout q, k, v, o, m;
   int64_t seg_bs, lse_bs, lse_hs;
   const void* Q;
@@ -61,19 +64,26 @@ __host__ __device__ __forceinline__ int64_t clamp64(int64_t x, int64_t lo, int64
   return x < lo ? lo : (x > hi ? hi : x);
 }
 
-// Visible key range [lo, hi) of query row i of batch entry b: the three
-// structural rules (key length, causal bound, segment start) intersect to one
-// interval.
+// Visible key range [lo, hi) of query row i of batch entry b: the structural
+// rules (key length, causal bound with its optional left window, segment
+// start) intersect to one interval.  L_b is the entry's valid key count; the
+// causal diagonal of row i is key i + off with off the problem's offset, or
+// L_b - Sq when the bound is right-aligned to the entry's length.
 __device__ __forceinline__ void row_range(const Problem& p, int b, int i, int64_t& lo, int64_t& hi) {
-  hi = p.Sk;
-  if (p.klens) hi = clamp64((int64_t)p.klens[b], 0, p.Sk);
-  if (p.causal) {
-    int64_t c = (int64_t)i + p.coff + 1;
-    hi = c < hi ? c : hi;
-    if (hi < 0) hi = 0;
-  }
+  int64_t kl = p.Sk;
+  if (p.klens) kl = clamp64((int64_t)p.klens[b] + p.klens_plus, 0, p.Sk);
+  hi = kl;
   lo = 0;
-  if (p.seg) lo = clamp64((int64_t)p.seg[(int64_t)b * p.seg_bs + i], 0, p.Sk);
+  if (p.causal) {
+    const int64_t diag = (int64_t)i + (p.align_klens ? kl - p.Sq : p.coff);
+    hi = diag + 1 < hi ? diag + 1 : hi;
+    if (hi < 0) hi = 0;
+    if (p.window >= 0 && diag - p.window > lo) lo = diag - p.window;
+  }
+  if (p.seg) {
+    const int64_t s = clamp64((int64_t)p.seg[(int64_t)b * p.seg_bs + i], 0, p.Sk);
+    if (s > lo) lo = s;
+  }
 }
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current

@@ -150,16 +150,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < C::kChunks; ++c)
         tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
   }
-  // The union of the rows' visible key ranges.  Without segment starts every
-  // range begins at key 0 and ends at a bound that does not decrease with the
-  // row, so the last valid row gives the union; otherwise reduce over rows.
+  // The union of the rows' visible key ranges.  Without segment starts both
+  // ends of a row's range are non-decreasing in the row (the window's left end
+  // moves with the diagonal), so [lo of the first row, hi of the last row)
+  // covers the union; otherwise reduce over rows.
   int lo_u, hi_u;
   if (p.seg == nullptr) {
     const int last = min(q0 + 2 * BM, p.Sq) - 1;
-    int64_t l64 = 0, h64 = 0;
-    if (last >= q0) row_range(p, b, last, l64, h64);
-    lo_u = 0;
-    hi_u = h64 > 0 ? (int)h64 : -1;
+    int64_t l64 = 0, h64 = 0, f_lo = 0, f_hi = 0;
+    if (last >= q0) {
+      row_range(p, b, last, l64, h64);
+      row_range(p, b, q0, f_lo, f_hi);
+    }
+    lo_u = (int)f_lo;
+    hi_u = h64 > f_lo ? (int)h64 : -1;
   } else {
     if (warp < 8 && hi > lo) {
       atomicMin(&sb.lo_u, lo);

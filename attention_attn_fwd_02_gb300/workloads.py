@@ -119,10 +119,13 @@ def doc_starts(seed: int, batch: int, seq: int, lo: int = 64, hi: int = 512) -> 
 def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, heads=2, kv_heads=None,
               q_len=16, k_len=None, head_dim=32, causal=False, causal_offset=None, scale=0.0,
               masked_rows="nan", value_scale=1.0, k_lens=None, seg=None, mask=None,
-              mask_kind="b11k", nan_fill=True, packed=False, decode=False) -> Case:
+              mask_kind="b11k", nan_fill=True, packed=False, decode=False, window_left=None,
+              causal_align="fixed", k_lens_kind="count") -> Case:
     """A general seeded problem.
 
-    k_lens / seg / mask may be arrays (used as given) or None.  mask_kind names
+    k_lens / seg / mask may be arrays (used as given) or None.  window_left,
+    causal_align and k_lens_kind are the visibility variants of the problem
+    (k_lens holds the values as passed: count - 1 under 'last_index').  mask_kind names
     the broadcast shape of a given mask: 'b11k' [B,1,1,K], 'bhqk' [B,H,Q,K],
     '11qk' [1,1,Q,K].  packed=True stores Q, K and V as slices of one
     [B, S, H + 2*KVH, D] projection (q_len must equal k_len).  decode=True
@@ -144,7 +147,7 @@ def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, head
         k_lens = np.asarray(k_lens, dtype=np.int32)
         if nan_fill:
             for b in range(B):
-                kl = int(min(max(int(k_lens[b]), 0), Sk))
+                kl = int(min(max(int(k_lens[b]) + (1 if k_lens_kind == "last_index" else 0), 0), Sk))
                 if kv_kind == "bshd" or packed:
                     kx[b, kl:] = np.nan
                     vx[b, kl:] = np.nan
@@ -153,7 +156,8 @@ def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, head
                     vx[b, :, kl:] = np.nan
     prob = dict(batch=B, heads=H, kv_heads=G, q_len=Sq, k_len=Sk, head_dim=D, dtype=dtype,
                 scale=float(scale), causal=bool(causal), causal_offset=causal_offset,
-                masked_rows=masked_rows)
+                masked_rows=masked_rows, window_left=window_left, causal_align=causal_align,
+                k_lens_kind=k_lens_kind)
     if packed:
         assert Sq == Sk and not decode
         W = H + 2 * G
@@ -257,18 +261,22 @@ def visible_pairs(case: Case) -> int:
     p = case.problem
     B, H, Sq, Sk = p["batch"], p["heads"], p["q_len"], p["k_len"]
     off = p["causal_offset"] if p["causal_offset"] is not None else Sk - Sq
+    plus = 1 if p.get("k_lens_kind") == "last_index" else 0
+    w = p.get("window_left")
     total = 0
     qi = np.arange(Sq, dtype=np.int64)
     for b in range(B):
-        hi = np.full(Sq, Sk, dtype=np.int64)
-        if case.k_lens is not None:
-            hi[:] = min(max(int(case.k_lens[b]), 0), Sk)
-        if p["causal"]:
-            hi = np.minimum(hi, np.maximum(qi + off + 1, 0))
+        kl = Sk if case.k_lens is None else min(max(int(case.k_lens[b]) + plus, 0), Sk)
+        hi = np.full(Sq, kl, dtype=np.int64)
         lo = np.zeros(Sq, dtype=np.int64)
+        if p["causal"]:
+            diag = qi + (kl - Sq if p.get("causal_align") == "klens" else off)
+            hi = np.minimum(hi, np.maximum(diag + 1, 0))
+            if w is not None and w >= 0:
+                lo = np.maximum(lo, diag - w)
         if case.seg is not None:
             s = case.seg if case.seg.ndim == 1 else case.seg[b]
-            lo = np.clip(s.astype(np.int64), 0, Sk)
+            lo = np.maximum(lo, np.clip(s.astype(np.int64), 0, Sk))
         if case.mask is None:
             total += H * int(np.maximum(hi - lo, 0).sum())
             continue

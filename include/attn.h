@@ -18,8 +18,11 @@
  * key lengths, additive attention bias with broadcast leading dimensions).
  *
  * Key visibility.  Key k (0 <= k < k_len) is visible to row (b, i) iff
- *   - k < clamp(k_lens[b], 0, k_len)          when k_lens is given, and
- *   - k <= i + causal_offset                  when causal != 0, and
+ *   - k < L_b = clamp(k_lens[b], 0, k_len)    when k_lens is given (L_b = k_len otherwise;
+ *                                             k_lens[b] + 1 under ATTN_KLENS_LAST_INDEX), and
+ *   - k <= i + off_b                          when causal != 0, with off_b = causal_offset,
+ *                                             or L_b - q_len under ATTN_CAUSAL_KLENS, and
+ *   - k >= i + off_b - window_left            when causal != 0 and window_left >= 0, and
  *   - k >= clamp(seg[b, i], 0, k_len)         when seg is given,
  * and its weight is zero when mask[b,h,i,k] = -inf.  A visible key whose score
  * is NaN or +inf makes the whole row NaN (O and LSE).  A row with no key of
@@ -72,7 +75,8 @@ enum { ATTN_MASKED_ROWS_NAN = 0, ATTN_MASKED_ROWS_ZERO = 1 };
 enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,    /* null required pointer, negative size, heads % kv_heads != 0,
-                                  head_dim outside [1, 256], odd head_dim for f16/bf16, bad layout */
+                                  head_dim outside [1, 256], odd head_dim for f16/bf16, bad layout,
+                                  window_left < -1 or a window without causal, unknown enum value */
   ATTN_ERR_UNSUPPORTED = 2,    /* a valid combination this build does not implement */
   ATTN_ERR_ALIGNMENT = 3,      /* a pointer not aligned to its element size */
   ATTN_ERR_WORKSPACE = 4,      /* workspace missing or smaller than the size query says */
@@ -83,6 +87,18 @@ enum {
 /* ATTN_OFFSET_DEFAULT as causal_offset selects k_len - q_len ("Attention",
  * section "What it covers": the cached-decoder default). */
 #define ATTN_OFFSET_DEFAULT INT64_MIN
+
+/* Where the causal diagonal sits ("com.microsoft.GroupQueryAttention",
+ * chunked-prefill variants: the causal bound of each sample is right-aligned
+ * to its live length).  ATTN_CAUSAL_FIXED: one offset for every batch entry
+ * (causal_offset).  ATTN_CAUSAL_KLENS: batch entry b's offset is L_b - q_len,
+ * so its last query row sees exactly its L_b valid keys. */
+enum { ATTN_CAUSAL_FIXED = 0, ATTN_CAUSAL_KLENS = 1 };
+
+/* Meaning of k_lens[b] ("com.microsoft.GroupQueryAttention", input seqlens_k):
+ * ATTN_KLENS_COUNT: the number of valid keys; ATTN_KLENS_LAST_INDEX: the index
+ * of the last valid key, i.e. the count minus one (ONNX seqlens_k as given). */
+enum { ATTN_KLENS_COUNT = 0, ATTN_KLENS_LAST_INDEX = 1 };
 
 /* A strided 4-D view [batch][head][row][element]: element (b, h, r, e) is at
  * base[offset + b*batch_stride + h*head_stride + r*row_stride + e].  Strides
@@ -110,6 +126,12 @@ typedef struct {
   int64_t seg_batch_stride;        /* seg is int32 [batch][q_len] with this batch stride (0 shares one row set) */
   int64_t lse_batch_stride;        /* LSE float32 element (b, h, i) at lse[b*lse_batch_stride + */
   int64_t lse_head_stride;         /*   h*lse_head_stride + i] */
+  /* Visibility variants ("com.microsoft.GroupQueryAttention", attribute
+   * local_window_size, input seqlens_k, chunked-prefill causal bound). */
+  int32_t window_left;             /* -1: off.  With causal, row i keeps keys i + off_b - window_left
+                                      .. i + off_b (window_left + 1 keys at most).  Requires causal. */
+  int32_t causal_align;            /* ATTN_CAUSAL_FIXED / ATTN_CAUSAL_KLENS */
+  int32_t k_lens_kind;             /* ATTN_KLENS_COUNT / ATTN_KLENS_LAST_INDEX */
 } attn_problem;
 
 /* Bytes of device workspace attn_fwd needs for this problem (0 when none).

@@ -46,13 +46,15 @@ def test_struct_layout_matches_c(tmp_path):
                    'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(attn_problem),'
                    ' offsetof(attn_problem, causal_offset), offsetof(attn_problem, q),'
                    ' offsetof(attn_problem, mask), offsetof(attn_problem, seg_batch_stride),'
-                   ' offsetof(attn_problem, lse_head_stride)); return 0;}\n')
+                   ' offsetof(attn_problem, lse_head_stride)); printf("%zu %zu %zu\\n",'
+                   ' offsetof(attn_problem, window_left), offsetof(attn_problem, causal_align),'
+                   ' offsetof(attn_problem, k_lens_kind)); return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.run(["gcc", str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     P = attn.attn_problem
     want = [ctypes.sizeof(P), P.causal_offset.offset, P.q.offset, P.mask.offset, P.seg_batch_stride.offset,
-            P.lse_head_stride.offset]
+            P.lse_head_stride.offset, P.window_left.offset, P.causal_align.offset, P.k_lens_kind.offset]
     assert got == want
 
 
@@ -79,13 +81,20 @@ FAKE = 0x10000  # never dereferenced: every case below fails on the host first
     (dict(q_layout=(0, -1, 64, 256)), attn.ATTN_ERR_INVALID_ARG),
     (dict(causal=2), attn.ATTN_ERR_INVALID_ARG),
     (dict(masked_rows=5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(window_left=3), attn.ATTN_ERR_INVALID_ARG),             # a window needs the causal bound
+    (dict(window_left=-2, causal=True), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal_align=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(k_lens_kind=3), attn.ATTN_ERR_INVALID_ARG),
 ])
 def test_fwd_rejects_invalid_problems(L, kw, code):
     p = base_problem(**kw)
     if "causal" in kw:
-        p.causal = kw["causal"]
+        p.causal = int(kw["causal"])
     if "masked_rows" in kw:
         p.masked_rows = kw["masked_rows"]
+    for name in ("causal_align", "k_lens_kind"):
+        if name in kw:
+            setattr(p, name, kw[name])
     assert attn.attn_fwd(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None, 0, None) == code
 
 
@@ -130,4 +139,4 @@ def test_status_strings_and_version(L):
     for code in range(7):
         assert attn.status_string(code) and attn.status_string(code) != "unknown status"
     assert attn.status_string(99) == "unknown status"
-    assert attn.attn_version() >= 100
+    assert attn.attn_version() >= 200

@@ -284,3 +284,57 @@ def test_decode_bounded_wait_reports_timeout_and_context_stays_usable(monkeypatc
     monkeypatch.delenv("ATTN_TEST_DROP_FIRST_COPY")
     assert attn.attn_device_status() == attn.ATTN_OK      # the status word was cleared
     run_and_compare(c)
+
+
+# ---- visibility variants: sliding window, right-aligned causal bound, last-index lengths -----------
+
+VIS = [
+    # dtype, layout, B, H, G, Sq, Sk, D, offset, window, align, lens, last_index, mask
+    ("bf16", "bhsd", 2, 8, 2, 300, 700, 128, None, 100, "klens", True, False, None),    # chunked prefill + window
+    ("bf16", "bshd", 2, 6, 3, 260, 260, 64, 0, 31, "fixed", False, False, None),         # sliding window, d64
+    ("bf16", "bhsd", 3, 4, 4, 200, 900, 64, None, -1, "klens", True, True, None),        # ONNX seqlens_k as given
+    ("f16", "bshd", 2, 4, 2, 150, 400, 256, None, 37, "klens", True, False, "b11k"),     # head_dim 256 + mask
+    ("f32", "bshd", 2, 2, 1, 70, 90, 32, 5, 9, "fixed", True, True, None),               # CUDA-core float32
+    ("f16", "bhsd", 1, 4, 2, 129, 129, 96, None, 0, "fixed", False, False, None),        # window 0, generic path
+]
+
+
+@pytest.mark.parametrize("i", range(len(VIS)))
+def test_visibility_variants(i):
+    dtype, layout, B, H, G, Sq, Sk, D, off, w, align, use_lens, last, mk = VIS[i]
+    r = np.random.default_rng(700 + i)
+    k_lens = None
+    if use_lens:
+        counts = r.integers(Sq, Sk + 1, size=B).astype(np.int32)
+        counts[0] = Sk
+        k_lens = counts - 1 if last else counts
+    mask = None
+    if mk is not None:
+        mask = r.standard_normal((B, 1, 1, Sk)).astype(np.float32)
+        mask[r.random(mask.shape) < 0.1] = -np.inf
+    c = wl.make_case(name=f"vis{i}", seed=800 + i, dtype=dtype, layout=layout, batch=B, heads=H, kv_heads=G,
+                     q_len=Sq, k_len=Sk, head_dim=D, causal=True, causal_offset=off, k_lens=k_lens, mask=mask,
+                     window_left=None if w < 0 else w, causal_align=align,
+                     k_lens_kind="last_index" if last else "count")
+    run_and_compare(c)
+
+
+def test_window_zero_returns_the_diagonal_value_exactly_on_the_tensor_core_path():
+    B, H, S, D = 2, 4, 300, 128
+    c = wl.make_case(name="win0", seed=91, dtype="bf16", layout="bhsd", batch=B, heads=H, q_len=S, head_dim=D,
+                     causal=True, causal_offset=0, window_left=0)
+    g = GpuCase(c).run()
+    _, _, raw = g.outputs()
+    assert np.array_equal(raw, c.v.reshape(B, H, S, D))
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_decode_sliding_window_and_last_index_lengths(D):
+    B, H, G, cap, w = 4, 16, 4, 3000, 700
+    r = np.random.default_rng(41 + D)
+    counts = r.integers(1, cap + 1, size=B).astype(np.int32)
+    counts[0] = 5
+    c = wl.make_case(name=f"decwin{D}", seed=43 + D, dtype="bf16", batch=B, heads=H, kv_heads=G, q_len=1,
+                     k_len=cap, head_dim=D, k_lens=counts - 1, decode=True, causal=True, window_left=w,
+                     causal_align="klens", k_lens_kind="last_index")
+    run_and_compare(c)
