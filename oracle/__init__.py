@@ -60,7 +60,9 @@ class _Problem(ctypes.Structure):
                 ("causal_offset", ctypes.c_int64), ("masked_rows_zero", ctypes.c_int32),
                 ("q", _Layout), ("k", _Layout), ("v", _Layout), ("mask", _Layout),
                 ("seg_batch_stride", ctypes.c_int64), ("window_left", ctypes.c_int32),
-                ("causal_align", ctypes.c_int32), ("k_lens_kind", ctypes.c_int32)]
+                ("causal_align", ctypes.c_int32), ("k_lens_kind", ctypes.c_int32),
+                ("softcap", ctypes.c_float), ("smooth_softmax", ctypes.c_int32),
+                ("head_sink", ctypes.c_void_p)]
 
 
 def _load():
@@ -100,7 +102,7 @@ def default_threads() -> int:
     return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
 
 
-def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nthreads=None):
+def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nthreads=None, head_sink=None):
     """O and LSE of the requested query rows, in float64.
 
     problem: dict with batch, heads, kv_heads, q_len, k_len, head_dim, dtype
@@ -108,7 +110,9 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
       k_len - q_len), masked_rows ('nan'|'zero'), q_layout/k_layout/v_layout
       and mask_layout as (offset, batch_stride, head_stride, row_stride) in
       elements, seg_batch_stride; optional window_left (None/-1 = off),
-      causal_align ('fixed' | 'klens'), k_lens_kind ('count' | 'last_index').
+      causal_align ('fixed' | 'klens'), k_lens_kind ('count' | 'last_index'),
+      softcap (0 = off), smooth_softmax (bool).
+    head_sink: None or float32 [heads] per-head sink logits.
     q, k, v: raw storage (float32 for f32, uint16 bit patterns for f16/bf16),
       indexed through the layouts.  mask: float32 storage; seg, k_lens: int32.
     rows: None for every (b, h, qi) row in that order, else an int array [n, 3].
@@ -139,6 +143,12 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
     prob.window_left = -1 if w is None else int(w)
     prob.causal_align = 1 if p.get("causal_align") in ("klens", 1) else 0
     prob.k_lens_kind = 1 if p.get("k_lens_kind") in ("last_index", 1) else 0
+    prob.softcap = float(p.get("softcap") or 0.0)
+    prob.smooth_softmax = 1 if p.get("smooth_softmax") else 0
+    sink = None if head_sink is None else np.ascontiguousarray(head_sink, dtype=np.float32)
+    if sink is not None and sink.shape != (p["heads"],):
+        raise ValueError("head_sink must be float32 [heads]")
+    prob.head_sink = None if sink is None else sink.ctypes.data
     if rows is None:
         n_rows = p["batch"] * p["heads"] * p["q_len"]
         rows_arr = None

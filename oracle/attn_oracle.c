@@ -46,6 +46,19 @@
  * its chunked-prefill variants, whose causal bound is right-aligned to each
  * sample's live length.
  *
+ * Score transforms, from the same page (attributes softcap and
+ * smooth_softmax, input head_sink), with these readings:
+ *   - soft-capping with cap c > 0 replaces the scaled dot product s by
+ *     c * tanh(s / c); the additive mask is added after it (so a -inf mask
+ *     still hides its key);
+ *   - the per-head sink value sigma_h is a logit that joins every row's
+ *     softmax denominator as exp(sigma_h) and adds nothing to the numerator;
+ *     smooth_softmax without per-head values uses sigma_h = 0 (the "+1" of the
+ *     smooth-softmax denominator).  LSE is the log of the whole denominator.
+ *     A row with a sink and no visible key therefore gives O = 0 and
+ *     LSE = sigma_h in both masked-rows modes; a NaN or +inf score (the sink
+ *     included) still makes the row NaN, and a sink of -inf adds nothing.
+ *
  * Precision: every product and sum is in double.  Inputs are read in their
  * storage type (float32, IEEE half or bfloat16 bit patterns) and widened
  * exactly to double.  The combine routine follows "Attention", section
@@ -78,6 +91,9 @@ typedef struct {
   int32_t window_left;    /* -1: no window; else causal rows keep keys >= i + offset - window_left */
   int32_t causal_align;   /* 0: one offset; 1: batch b's offset is its clamped key length - q_len */
   int32_t k_lens_kind;    /* 0: k_lens are counts; 1: they are the last valid index (count - 1) */
+  float softcap;          /* 0: off; > 0: scores are softcap * tanh(scale q.k / softcap) before the mask */
+  int32_t smooth_softmax; /* 1: a sink logit joins each row's denominator (sigma = 0 unless head_sink) */
+  const float* head_sink; /* NULL or float [heads]: per-head sink logits (turns the sink on) */
 } orc_problem;
 
 /* ---- exact widening of the storage types --------------------------------- */
@@ -189,6 +205,10 @@ static void orc_row(const orc_job* j, int64_t b, int64_t h, int64_t qi,
     for (int64_t d = 0; d < D; ++d)
       dot += orc_load(j->q, p->dtype, qbase + d) * orc_load(j->k, p->dtype, kbase + d);
     double sc = scale * dot;
+    if (p->softcap > 0.0f) {
+      const double cap = (double)p->softcap;
+      sc = cap * tanh(sc / cap);
+    }
     if (j->mask) {
       const int64_t mbase = p->mask.offset + b * p->mask.batch_stride + h * p->mask.head_stride +
                             qi * p->mask.row_stride;
@@ -198,7 +218,12 @@ static void orc_row(const orc_job* j, int64_t b, int64_t h, int64_t qi,
     if (isnan(sc) || (isinf(sc) && sc > 0)) any_nan_or_pinf = 1;
   }
 
-  /* Pass 1: classify the row and find the maximum over the keys with weight > 0. */
+  /* Pass 1: classify the row and find the maximum over the keys with weight > 0
+   * (and the sink logit, when there is one). */
+  const double sigma = p->head_sink ? (double)p->head_sink[h] : 0.0;
+  int sink_on = p->smooth_softmax || p->head_sink != NULL;
+  if (sink_on && (isnan(sigma) || sigma == INFINITY)) any_nan_or_pinf = 1;   /* the sink is a score too */
+  if (sink_on && sigma == -INFINITY) sink_on = 0;                               /* exp(-inf) adds nothing */
   if (any_nan_or_pinf) {
     for (int64_t d = 0; d < D; ++d) o_row[d] = NAN;
     *lse_out = NAN;
@@ -211,16 +236,18 @@ static void orc_row(const orc_job* j, int64_t b, int64_t h, int64_t qi,
     if (!any || s[kk] > m) m = s[kk];
     any = 1;
   }
-  if (!any) {                                  /* no visible key: NaN, or 0 under MaskedRows = Zero */
+  if (!any && !sink_on) {                      /* no visible key: NaN, or 0 under MaskedRows = Zero */
     for (int64_t d = 0; d < D; ++d) o_row[d] = p->masked_rows_zero ? 0.0 : NAN;
     *lse_out = -INFINITY;
     return;
   }
+  if (sink_on && (!any || sigma > m)) m = sigma;
 
-  /* Pass 2: l = sum of exp(s - m), increasing key order. */
+  /* Pass 2: l = sum of exp(s - m), increasing key order, then the sink term. */
   double l = 0.0;
   for (int64_t kk = 0; kk < p->k_len; ++kk)
     if (vis[kk] && s[kk] > -INFINITY) l += exp(s[kk] - m);
+  if (sink_on) l += exp(sigma - m);
 
   /* Pass 3: O = sum of exp(s - m) V[k] / l; LSE = m + log(l). */
   for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;
