@@ -42,7 +42,8 @@ class attn_problem(ctypes.Structure):
                 ("mask", attn_layout), ("seg_batch_stride", ctypes.c_int64),
                 ("lse_batch_stride", ctypes.c_int64), ("lse_head_stride", ctypes.c_int64),
                 ("window_left", ctypes.c_int32), ("causal_align", ctypes.c_int32),
-                ("k_lens_kind", ctypes.c_int32)]
+                ("k_lens_kind", ctypes.c_int32), ("softcap", ctypes.c_float),
+                ("smooth_softmax", ctypes.c_int32), ("head_sink", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):
@@ -159,6 +160,9 @@ def make_problem(d: dict) -> attn_problem:
     p.causal_align = ATTN_CAUSAL_KLENS if d.get("causal_align") in ("klens", ATTN_CAUSAL_KLENS) else ATTN_CAUSAL_FIXED
     p.k_lens_kind = (ATTN_KLENS_LAST_INDEX if d.get("k_lens_kind") in ("last_index", ATTN_KLENS_LAST_INDEX)
                      else ATTN_KLENS_COUNT)
+    p.softcap = float(d.get("softcap") or 0.0)
+    p.smooth_softmax = 1 if d.get("smooth_softmax") else 0
+    p.head_sink = d.get("head_sink_ptr")      # device address of float32 [heads], or None
     return p
 
 
@@ -193,13 +197,15 @@ def _check(code, where):
 
 def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, mask=None, seg=None,
         k_lens=None, masked_rows="nan", return_lse=False, out=None, lse=None, stream=None,
-        window_left=None, causal_align="fixed", k_lens_kind="count"):
+        window_left=None, causal_align="fixed", k_lens_kind="count", softcap=0.0, smooth_softmax=False,
+        head_sink=None):
     """O (and LSE) for torch CUDA tensors.  layout 'bshd': Q [B,Sq,H,D], K/V [B,Sk,G,D];
     'bhsd': Q [B,H,Sq,D], K/V [B,G,Sk,D].  mask: float32 broadcastable 4-D [B|1, H|1, Sq|1, Sk]
     with contiguous keys; seg: int32 [B, Sq] or [Sq]; k_lens: int32 [B].  window_left: left
     window of causal local attention (None = off); causal_align: 'fixed' (one offset) or
     'klens' (each entry's diagonal right-aligned to its key length); k_lens_kind: 'count' or
-    'last_index' (ONNX seqlens_k, count minus one)."""
+    'last_index' (ONNX seqlens_k, count minus one).  softcap: cap of the scaled scores (0 = off);
+    smooth_softmax / head_sink (float32 [H] CUDA tensor): the sink term of the denominator."""
     torch = _torch()
     hd = 2 if layout == "bshd" else 1
     sd = 1 if layout == "bshd" else 2
@@ -211,7 +217,8 @@ def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, 
              causal=causal, causal_offset=causal_offset, masked_rows=masked_rows,
              q_layout=_layout4(q, hd), k_layout=_layout4(k, hd), v_layout=_layout4(v, hd),
              o_layout=_layout4(out, hd), window_left=window_left, causal_align=causal_align,
-             k_lens_kind=k_lens_kind)
+             k_lens_kind=k_lens_kind, softcap=softcap, smooth_softmax=smooth_softmax,
+             head_sink_ptr=_ptr(head_sink))
     if mask is not None:
         if mask.dtype != torch.float32 or mask.dim() != 4 or mask.stride(3) != 1:
             raise ValueError("mask must be float32, 4-D, keys contiguous")
@@ -233,7 +240,8 @@ def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, 
 
 
 def decode(q, k_cache, v_cache, k_lens=None, *, scale=0.0, mask=None, masked_rows="nan", return_lse=False,
-           out=None, lse=None, workspace=None, stream=None, window_left=None, k_lens_kind="count"):
+           out=None, lse=None, workspace=None, stream=None, window_left=None, k_lens_kind="count", softcap=0.0,
+           smooth_softmax=False, head_sink=None):
     """Single-query decode: q [B, 1, H, D]; caches BNSH [B, G, cap, D]; k_lens int32 [B].
     window_left keeps only the last window_left + 1 valid keys (local attention);
     k_lens_kind 'last_index' takes ONNX seqlens_k (count minus one) as given."""
@@ -244,7 +252,8 @@ def decode(q, k_cache, v_cache, k_lens=None, *, scale=0.0, mask=None, masked_row
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     d = dict(batch=B, heads=H, kv_heads=G, q_len=Sq, k_len=cap, head_dim=D, dtype=_dtype_name(q), scale=scale,
              causal=window_left is not None, causal_align="klens", window_left=window_left,
-             k_lens_kind=k_lens_kind, masked_rows=masked_rows, q_layout=_layout4(q, 2),
+             k_lens_kind=k_lens_kind, softcap=softcap, smooth_softmax=smooth_softmax,
+             head_sink_ptr=_ptr(head_sink), masked_rows=masked_rows, q_layout=_layout4(q, 2),
              k_layout=_layout4(k_cache, 1), v_layout=_layout4(v_cache, 1), o_layout=_layout4(out, 2))
     if mask is not None:
         d["mask_layout"] = (0, mask.stride(0) if mask.shape[0] > 1 else 0,

@@ -63,6 +63,9 @@ int check_problem(const attn_problem* p) {
   if (p->window_left < -1 || (p->window_left >= 0 && !p->causal)) return ATTN_ERR_INVALID_ARG;
   if (p->causal_align != ATTN_CAUSAL_FIXED && p->causal_align != ATTN_CAUSAL_KLENS) return ATTN_ERR_INVALID_ARG;
   if (p->k_lens_kind != ATTN_KLENS_COUNT && p->k_lens_kind != ATTN_KLENS_LAST_INDEX) return ATTN_ERR_INVALID_ARG;
+  if (!(p->softcap >= 0.0f) || isinf(p->softcap)) return ATTN_ERR_INVALID_ARG;
+  if (p->smooth_softmax != 0 && p->smooth_softmax != 1) return ATTN_ERR_INVALID_ARG;
+  if (p->head_sink && !aligned(p->head_sink, 4)) return ATTN_ERR_ALIGNMENT;
   return ATTN_OK;
 }
 
@@ -85,6 +88,9 @@ Problem resolve(const attn_problem* p, const void* q, const void* k, const void*
   r.window = p->window_left;
   r.align_klens = p->causal_align == ATTN_CAUSAL_KLENS;
   r.klens_plus = p->k_lens_kind == ATTN_KLENS_LAST_INDEX ? 1 : 0;
+  r.softcap = p->softcap;
+  r.sink_on = (p->smooth_softmax || p->head_sink) ? 1 : 0;
+  r.sink = p->head_sink;
   r.q = {p->q.offset, p->q.batch_stride, p->q.head_stride, p->q.row_stride};
   r.k = {p->k.offset, p->k.batch_stride, p->k.head_stride, p->k.row_stride};
   r.v = {p->v.offset, p->v.batch_stride, p->v.head_stride, p->v.row_stride};
@@ -258,6 +264,6 @@ const char* attn_status_string(int status) {
   }
 }
 
-int attn_version(void) { return 200; }
+int attn_version(void) { return 210; }
 
 }  // extern "C"

@@ -27,6 +27,9 @@ struct Problem {
   int window;                    // left window (keys behind the diagonal), -1 = none
   int align_klens;               // 1: causal offset of entry b is L_b - Sq
   int klens_plus;                // added to k_lens[b] (1 for last-index lengths)
+  float softcap;                 // 0: off; > 0: scores are softcap * tanh(scale q.k / softcap)
+  int sink_on;                   // 1: a sink logit joins every row's denominator
+  const float* sink;             // per-head sink logits (nullptr: 0 for every head)
   Layout q, k, v, o, m;
   int64_t seg_bs, lse_bs, lse_hs;
   const void* Q;
@@ -84,6 +87,44 @@ __device__ __forceinline__ void row_range(const Problem& p, int b, int i, int64_
     const int64_t s = clamp64((int64_t)p.seg[(int64_t)b * p.seg_bs + i], 0, p.Sk);
     if (s > lo) lo = s;
   }
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh(y) from its definition with a single base-2 exponential:
+// tanh(|y|) = (1 - e) / (1 + e) with e = exp(-2|y|) = 2^(-2 log2(e) |y|), and
+// the sign of y restored.  The subtraction 1 - e costs at most one float32
+// ulp of 1 in absolute error near y = 0; large |y| gives e = 0 and +-1; NaN
+// stays NaN.  Used by the half-precision kernels' soft-capping.
+__device__ __forceinline__ float tanh_exp2(float y) {
+  const float e = ex2_approx(-2.8853900817779268f * fabsf(y));
+  return copysignf(__fdividef(1.f - e, 1.f + e), y);
+}
+
+// The sink logit of head h in natural-log units.
+__device__ __forceinline__ float sink_logit(const Problem& p, int h) { return p.sink ? p.sink[h] : 0.f; }
+
+// Folds a sink logit s (same units and base as m) into a row's running
+// maximum m and sum l, where the row's sum is l relative to m and base is 2
+// (exp2) or e (exp): afterwards l and m describe the row including the sink,
+// and the returned factor rescales the row's accumulated numerator.  A NaN or
+// +inf sink makes the row NaN; a -inf sink changes nothing.
+template <bool BASE2>
+__device__ __forceinline__ float fold_sink(float& m, float& l, float s) {
+  if (s != s || s == INFINITY) {
+    l = NAN;
+    return 1.f;
+  }
+  if (s == -INFINITY) return 1.f;
+  const float mx = fmaxf(m, s);   // m = -inf (no visible key): the sink alone
+  const float f = BASE2 ? ex2_approx(m - mx) : expf(m - mx);
+  l = fmaf(l, f, BASE2 ? ex2_approx(s - mx) : expf(s - mx));
+  m = mx;
+  return f;
 }
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current

@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const __grid_const
     }
   }
   const float c = p.scale * kLog2e;
+  const bool capped = p.softcap > 0.f;
+  const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
   const float* mrow = p.M ? p.M + p.m.off + (int64_t)b * p.m.bs : nullptr;
 
   float o[16][4];
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const __grid_const
       for (int e = 0; e < 4; ++e) {
         const int64_t key = k0 + nt * 8 + tig * 2 + (e & 1);
         const int hh = gid + (e >> 1) * 8;
-        float x = sc[nt][e] * c;
+        float x = capped ? cap2 * tanh_exp2(sc[nt][e] * kinv) : sc[nt][e] * c;
         if (mrow && key < end && hh < nh) x = fmaf(mrow[(int64_t)(h0 + hh) * p.m.hs + key], kLog2e, x);
         sc[nt][e] = key < end ? x : -INFINITY;
       }

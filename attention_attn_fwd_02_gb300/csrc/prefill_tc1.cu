@@ -336,7 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return wait_warp(pair_bar, (uint32_t)phase & 1u, &sb.abort, p.status);
     };
     const float sc = p.scale * kLog2e;
-    const bool explicit_x = MASK || !(sc > 0.f);
+    // Soft-capping: the scaled product s becomes cap2 * tanh(s_raw * kinv) in log2 units.
+    const bool capped = p.softcap > 0.f;
+    const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
+    const bool explicit_x = MASK || !(sc > 0.f) || capped;
     const float c_eff = explicit_x ? 1.f : sc;
     const float* mrow = nullptr;
     if (MASK && qrow < p.Sq)
@@ -382,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < kHalf; ++e) {
           const int kk = k0 + e;
           const float s = __uint_as_float(x[e]);
-          const float v = MASK ? fmaf(s, sc, mv[e] * kLog2e) : s * sc;
+          const float t = capped ? cap2 * tanh_exp2(s * kinv) : s * sc;
+          const float v = MASK ? fmaf(mv[e], kLog2e, t) : t;
           x[e] = __float_as_uint((kk >= lo && kk < hi) ? v : -INFINITY);
         }
       } else if (!(k0 >= lo && k0 + kHalf <= hi)) {
@@ -473,12 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       fence_after();
       const bool valid = qrow < p.Sq;
+      // The sink logit joins the denominator (and rescales the accumulated O).
+      const float o_mul = p.sink_on ? fold_sink<true>(m_ref, l, sink_logit(p, h) * kLog2e) : 1.f;
       const bool hidden_row = (l == 0.f);  // no visible key; a NaN l stays a NaN row
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* orow = valid ? static_cast<T*>(p.O) + p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs +
                             (int64_t)qrow * p.o.rs + ch * (D / 2)
                       : nullptr;
-      const float inv = 1.f / l;
+      const float inv = o_mul / l;
       const float fill = p.masked_zero ? 0.f : NAN;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {

@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp
       const int kk = t0 + j;
       const bool vis = valid && kk >= lo && kk < hi;
       float x = p.scale * part;
+      if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap);
       if (vis && p.M) x += p.M[mrow + kk];
       sc[j] = vis ? x : -INFINITY;
       mt = fmaxf(mt, sc[j]);
@@ -152,8 +153,16 @@ __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp
   }
 
   if (!valid) return;
+  // Direct output (prefill) or one key range's partial result (decode: the
+  // combine merges the ranges and adds the sink term once).
+  const bool direct = sp.part_o == nullptr;
+  if (direct && p.sink_on) {
+    const float f = fold_sink<false>(m, l, sink_logit(p, h));
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) acc[s] *= f;
+  }
   const bool hidden = (l == 0.f);  // no key with non-zero weight; NaN l is a NaN row
-  if (sp.n_splits == 1) {
+  if (direct) {
     T* O = static_cast<T*>(p.O);
     const int64_t ob = p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs + (int64_t)i * p.o.rs;
     const float fill = p.masked_zero ? 0.f : NAN;
@@ -177,11 +186,14 @@ __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp
 }
 
 // One warp per row: merge the row's range partials in range order.
+// With sink_on the head's sink logit enters as one more range with an
+// empty numerator (the sink term of the denominator, added once per row).
 template <typename T>
 __global__ void __launch_bounds__(128) combine_kernel(int n_splits, int64_t rows, int D, const float* part_o,
                                                       const float* part_lse, T* O, Layout ol, int H, int Sq,
                                                       float* lse, int64_t lse_bs, int64_t lse_hs,
-                                                      int64_t lse_rs, int masked_zero) {
+                                                      int64_t lse_rs, int masked_zero, int sink_on,
+                                                      const float* sink) {
   const int64_t row = (int64_t)blockIdx.x * 4 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= rows) return;
@@ -195,6 +207,9 @@ __global__ void __launch_bounds__(128) combine_kernel(int n_splits, int64_t rows
   }
   const int i = (int)(row % Sq);
   const int h = (int)((row / Sq) % H);
+  const float sg = sink_on ? (sink ? sink[h] : 0.f) : -INFINITY;
+  if (isnan(sg) || sg == INFINITY) bad = true;
+  else M = fmaxf(M, sg);
   const int64_t b = row / ((int64_t)Sq * H);
   const int64_t ob = ol.off + b * ol.bs + (int64_t)h * ol.hs + (int64_t)i * ol.rs;
   float acc[8];
@@ -202,6 +217,7 @@ __global__ void __launch_bounds__(128) combine_kernel(int n_splits, int64_t rows
   for (int s = 0; s < 8; ++s) acc[s] = 0.f;
   float ws = 0.f;
   if (!bad && M != -INFINITY) {
+    if (sg > -INFINITY) ws = expf(sg - M);
     for (int r = 0; r < n_splits; ++r) {
       const float x = pl[r];
       if (x == -INFINITY) continue;
@@ -254,26 +270,28 @@ cudaError_t launch_simt_d(const Problem& p, const Split& s, cudaStream_t st) {
 template <typename T>
 cudaError_t launch_combine_t(int n_splits, int64_t rows, int D, const float* po, const float* pl, void* o,
                              Layout ol, int H, int Sq, float* lse, int64_t lbs, int64_t lhs, int64_t lrs,
-                             int masked_zero, cudaStream_t st) {
+                             int masked_zero, int sink_on, const float* sink, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int64_t blocks = (rows + 3) / 4;
   if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
   combine_kernel<T><<<(unsigned)blocks, 128, 0, st>>>(n_splits, rows, D, po, pl, static_cast<T*>(o), ol, H, Sq,
-                                                      lse, lbs, lhs, lrs, masked_zero);
+                                                      lse, lbs, lhs, lrs, masked_zero, sink_on, sink);
   return cudaGetLastError();
 }
 
 cudaError_t combine_dispatch(int32_t dt, int n_splits, int64_t rows, int D, const float* po, const float* pl,
                              void* o, Layout ol, int H, int Sq, float* lse, int64_t lbs, int64_t lhs,
-                             int64_t lrs, int masked_zero, cudaStream_t st) {
+                             int64_t lrs, int masked_zero, int sink_on, const float* sink, cudaStream_t st) {
   switch (dt) {
     case ATTN_F32:
-      return launch_combine_t<float>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs, masked_zero, st);
+      return launch_combine_t<float>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs, masked_zero,
+                                     sink_on, sink, st);
     case ATTN_F16:
-      return launch_combine_t<__half>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs, masked_zero, st);
+      return launch_combine_t<__half>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs, masked_zero,
+                                      sink_on, sink, st);
     default:
       return launch_combine_t<__nv_bfloat16>(n_splits, rows, D, po, pl, o, ol, H, Sq, lse, lbs, lhs, lrs,
-                                             masked_zero, st);
+                                             masked_zero, sink_on, sink, st);
   }
 }
 
@@ -290,7 +308,7 @@ cudaError_t launch_simt(const Problem& p, const Split& s, cudaStream_t st) {
 cudaError_t launch_combine(const Problem& p, const Split& s, int32_t out_dtype, cudaStream_t st) {
   const int64_t rows = (int64_t)p.B * p.H * p.Sq;
   return combine_dispatch(out_dtype, s.n_splits, rows, p.D, s.part_o, s.part_lse, p.O, p.o, p.H, p.Sq, p.lse,
-                          p.lse_bs, p.lse_hs, 1, p.masked_zero, st);
+                          p.lse_bs, p.lse_hs, 1, p.masked_zero, p.sink_on, p.sink, st);
 }
 
 cudaError_t launch_combine_flat(int n_splits, int rows, int D, const float* part_o, const float* part_lse,
@@ -298,7 +316,7 @@ cudaError_t launch_combine_flat(int n_splits, int rows, int D, const float* part
                                 cudaStream_t st) {
   Layout ol{0, 0, 0, o_row_stride};
   return combine_dispatch(out_dtype, n_splits, rows, D, part_o, part_lse, o, ol, 1, rows, lse, 0, 0, 1,
-                          masked_zero, st);
+                          masked_zero, 0, nullptr, st);
 }
 
 }  // namespace attn

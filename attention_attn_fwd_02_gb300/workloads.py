@@ -99,6 +99,7 @@ class Case:
     mask: np.ndarray | None = None
     seg: np.ndarray | None = None
     k_lens: np.ndarray | None = None
+    head_sink: np.ndarray | None = None
     decode: bool = False
     meta: dict = field(default_factory=dict)
 
@@ -120,7 +121,8 @@ def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, head
               q_len=16, k_len=None, head_dim=32, causal=False, causal_offset=None, scale=0.0,
               masked_rows="nan", value_scale=1.0, k_lens=None, seg=None, mask=None,
               mask_kind="b11k", nan_fill=True, packed=False, decode=False, window_left=None,
-              causal_align="fixed", k_lens_kind="count") -> Case:
+              causal_align="fixed", k_lens_kind="count", softcap=0.0, smooth_softmax=False,
+              head_sink=None) -> Case:
     """A general seeded problem.
 
     k_lens / seg / mask may be arrays (used as given) or None.  window_left,
@@ -157,7 +159,7 @@ def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, head
     prob = dict(batch=B, heads=H, kv_heads=G, q_len=Sq, k_len=Sk, head_dim=D, dtype=dtype,
                 scale=float(scale), causal=bool(causal), causal_offset=causal_offset,
                 masked_rows=masked_rows, window_left=window_left, causal_align=causal_align,
-                k_lens_kind=k_lens_kind)
+                k_lens_kind=k_lens_kind, softcap=float(softcap), smooth_softmax=bool(smooth_softmax))
     if packed:
         assert Sq == Sk and not decode
         W = H + 2 * G
@@ -194,8 +196,10 @@ def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, head
         seg = np.ascontiguousarray(seg, dtype=np.int32)
         prob["seg_batch_stride"] = 0 if seg.ndim == 1 else Sq
     prob["lse_layout"] = (H * Sq, Sq)   # LSE [B, H, q_len] float32
+    if head_sink is not None:
+        head_sink = np.ascontiguousarray(head_sink, dtype=np.float32)
     return Case(name=name, problem=prob, q=q, k=k, v=v, o_shape=o_shape, mask=mask, seg=seg,
-                k_lens=k_lens, decode=decode)
+                k_lens=k_lens, head_sink=head_sink, decode=decode)
 
 
 # ---- the five named workloads -------------------------------------------------

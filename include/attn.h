@@ -30,6 +30,15 @@
  * under ATTN_MASKED_ROWS_ZERO, and LSE = -inf.  Out-of-range k_lens and seg
  * values are clamped to [0, k_len] (a convention of this library).
  *
+ * Score transforms ("com.microsoft.GroupQueryAttention", attributes softcap
+ * and smooth_softmax, input head_sink).  With softcap c > 0 the scaled dot
+ * product s becomes c * tanh(s / c) before the mask is added.  With a sink,
+ * the logit sigma_h (head_sink[h], or 0 under smooth_softmax alone) joins
+ * every row's denominator as exp(sigma_h) and adds nothing to the numerator;
+ * LSE is the log of the whole denominator.  A row with a sink and no visible
+ * key gives O = 0 and LSE = sigma_h; a NaN or +inf sink makes the row NaN; a
+ * sink of -inf adds nothing.
+ *
  * Memory.  Every data pointer is a DEVICE pointer owned by the caller.  The
  * library allocates no device memory: scratch space is the caller's
  * `workspace` (size from the *_workspace_size queries).  K/V values of keys
@@ -76,7 +85,8 @@ enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,    /* null required pointer, negative size, heads % kv_heads != 0,
                                   head_dim outside [1, 256], odd head_dim for f16/bf16, bad layout,
-                                  window_left < -1 or a window without causal, unknown enum value */
+                                  window_left < -1 or a window without causal, unknown enum value,
+                                  negative or non-finite softcap */
   ATTN_ERR_UNSUPPORTED = 2,    /* a valid combination this build does not implement */
   ATTN_ERR_ALIGNMENT = 3,      /* a pointer not aligned to its element size */
   ATTN_ERR_WORKSPACE = 4,      /* workspace missing or smaller than the size query says */
@@ -132,6 +142,11 @@ typedef struct {
                                       .. i + off_b (window_left + 1 keys at most).  Requires causal. */
   int32_t causal_align;            /* ATTN_CAUSAL_FIXED / ATTN_CAUSAL_KLENS */
   int32_t k_lens_kind;             /* ATTN_KLENS_COUNT / ATTN_KLENS_LAST_INDEX */
+  /* Score transforms (see above). */
+  float softcap;                   /* 0: off; > 0: cap of the scaled dot products (finite) */
+  int32_t smooth_softmax;          /* 1: the sink term is on, sigma_h = 0 unless head_sink is given */
+  const float* head_sink;          /* nullable DEVICE pointer, float32 [heads]: per-head sink logits;
+                                      non-NULL turns the sink term on.  Owned by the caller. */
 } attn_problem;
 
 /* Bytes of device workspace attn_fwd needs for this problem (0 when none).

@@ -66,7 +66,8 @@ class GpuCase:
         B, H, Sq = p["batch"], p["heads"], p["q_len"]
         self.lse_buf = torch.full((B * H * Sq + 2 * guard,), 777.0, dtype=torch.float32, device="cuda") if lse else None
         self.lse = self.lse_buf[guard:guard + B * H * Sq] if lse else None
-        self.prob = attn.make_problem(p)
+        self.sink = dev(case.head_sink)
+        self.prob = attn.make_problem(dict(p, head_sink_ptr=None if self.sink is None else self.sink.data_ptr()))
         self.ws = None
         self.ws_bytes = 0
 
@@ -120,7 +121,8 @@ class GpuCase:
 
 def oracle_full(case: wl.Case):
     p = case.problem
-    o, lse = oracle.attn(p, case.q, case.k, case.v, mask=case.mask, seg=case.seg, k_lens=case.k_lens)
+    o, lse = oracle.attn(p, case.q, case.k, case.v, mask=case.mask, seg=case.seg, k_lens=case.k_lens,
+                         head_sink=case.head_sink)
     B, H, Sq, D = p["batch"], p["heads"], p["q_len"], p["head_dim"]
     return o.reshape(B, H, Sq, D), lse.reshape(B, H, Sq)
 

@@ -338,3 +338,60 @@ def test_decode_sliding_window_and_last_index_lengths(D):
                      k_len=cap, head_dim=D, k_lens=counts - 1, decode=True, causal=True, window_left=w,
                      causal_align="klens", k_lens_kind="last_index")
     run_and_compare(c)
+
+
+# ---- score transforms: soft-capping and the softmax sink ----------------------------------------
+
+TRANSFORMS = [
+    # dtype, layout, B, H, G, Sq, Sk, D, causal offset (None: not causal), softcap, sink, mask
+    ("bf16", "bhsd", 2, 8, 2, 300, 300, 128, 0, 1.0, "heads", None),        # head_dim 128, cap + sink
+    ("bf16", "bshd", 2, 6, 3, 200, 333, 64, None, 2.0, "none", "b11k"),      # head_dim 64, cap + mask
+    ("f16", "bshd", 2, 4, 2, 150, 400, 256, -60, 0.0, "smooth", "b11k"),     # head_dim 256, smooth softmax,
+                                                                             # first rows see no key
+    ("f16", "bshd", 1, 4, 4, 129, 300, 256, None, 1.5, "heads", None),       # head_dim 256, cap + sink
+    ("f32", "bshd", 2, 2, 1, 70, 90, 32, 3, 2.0, "heads", "bhqk"),           # CUDA-core float32
+    ("f16", "bhsd", 1, 4, 2, 129, 129, 96, 0, 0.0, "heads", None),           # CUDA-core half path
+]
+
+
+def transform_case(i, spec, decode=False):
+    dtype, layout, B, H, G, Sq, Sk, D, off, cap, sink, mk = spec
+    r = np.random.default_rng(900 + i)
+    mask = None
+    if mk is not None:
+        shape = {"b11k": (B, 1, 1, Sk), "bhqk": (B, H, Sq, Sk)}[mk]
+        mask = r.standard_normal(shape).astype(np.float32)
+        mask[r.random(shape) < 0.1] = -np.inf
+    head_sink = (r.standard_normal(H) * 2).astype(np.float32) if sink == "heads" else None
+    k_lens = r.integers(1, Sk + 1, size=B).astype(np.int32) if decode else None
+    return wl.make_case(name=f"tf{i}", seed=950 + i, dtype=dtype, layout=layout, batch=B, heads=H, kv_heads=G,
+                        q_len=Sq, k_len=Sk, head_dim=D, causal=off is not None, causal_offset=off, mask=mask,
+                        mask_kind=mk or "b11k", softcap=cap, smooth_softmax=sink == "smooth",
+                        head_sink=head_sink, k_lens=k_lens, decode=decode)
+
+
+@pytest.mark.parametrize("i", range(len(TRANSFORMS)))
+def test_softcap_and_sink(i):
+    st, _ = run_and_compare(transform_case(i, TRANSFORMS[i]))
+    assert st["nan_rows"] == 0      # with a sink a row without keys gives O = 0, not NaN
+
+
+DECODE_TF = [
+    # dtype, layout, B, H, G, Sq, Sk (capacity), D, offset, softcap, sink, mask
+    ("bf16", "bshd", 3, 16, 4, 1, 2000, 128, None, 1.5, "heads", "b11k"),   # tensor-core split pass
+    ("f16", "bshd", 2, 8, 2, 1, 900, 64, None, 0.0, "smooth", None),        # generic split pass
+    ("bf16", "bshd", 2, 6, 3, 1, 100, 64, None, 2.0, "heads", None),        # one key range, generic pass
+]
+
+
+@pytest.mark.parametrize("i", range(len(DECODE_TF)))
+def test_decode_softcap_and_sink(i):
+    run_and_compare(transform_case(100 + i, DECODE_TF[i], decode=True))
+
+
+def test_decode_single_range_generic_pass():
+    """A cache of at most 128 keys is one key range; the generic pass writes its
+    partial result for the combine like any other range."""
+    c = wl.make_case(name="dec1r", seed=977, dtype="f16", batch=3, heads=4, kv_heads=2, q_len=1, k_len=96,
+                     head_dim=64, k_lens=np.array([96, 1, 50], dtype=np.int32), decode=True)
+    run_and_compare(c)
