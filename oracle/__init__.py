@@ -62,7 +62,8 @@ class _Problem(ctypes.Structure):
                 ("seg_batch_stride", ctypes.c_int64), ("window_left", ctypes.c_int32),
                 ("causal_align", ctypes.c_int32), ("k_lens_kind", ctypes.c_int32),
                 ("softcap", ctypes.c_float), ("smooth_softmax", ctypes.c_int32),
-                ("head_sink", ctypes.c_void_p)]
+                ("head_sink", ctypes.c_void_p), ("kv_int8", ctypes.c_int32),
+                ("kv_per_channel", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 def _load():
@@ -102,7 +103,8 @@ def default_threads() -> int:
     return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
 
 
-def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nthreads=None, head_sink=None):
+def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nthreads=None, head_sink=None,
+         k_scale=None, v_scale=None):
     """O and LSE of the requested query rows, in float64.
 
     problem: dict with batch, heads, kv_heads, q_len, k_len, head_dim, dtype
@@ -113,6 +115,9 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
       causal_align ('fixed' | 'klens'), k_lens_kind ('count' | 'last_index'),
       softcap (0 = off), smooth_softmax (bool).
     head_sink: None or float32 [heads] per-head sink logits.
+    k_scale, v_scale: float32 scales when problem['kv_dtype'] == 'i8' (k and v are
+      then int8 storage): one value (problem['kv_scale'] == 'tensor') or
+      kv_heads * head_dim values ('channel').
     q, k, v: raw storage (float32 for f32, uint16 bit patterns for f16/bf16),
       indexed through the layouts.  mask: float32 storage; seg, k_lens: int32.
     rows: None for every (b, h, qi) row in that order, else an int array [n, 3].
@@ -121,7 +126,14 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
     lib = _load()
     p = problem
     dt = p["dtype"]
-    q, k, v = _storage(q, dt), _storage(k, dt), _storage(v, dt)
+    kv8 = p.get("kv_dtype") == "i8"
+    q = _storage(q, dt)
+    if kv8:
+        if np.asarray(k).dtype != np.int8 or np.asarray(v).dtype != np.int8:
+            raise TypeError("oracle expects int8 key/value storage for kv_dtype 'i8'")
+        k, v = np.ascontiguousarray(k), np.ascontiguousarray(v)
+    else:
+        k, v = _storage(k, dt), _storage(v, dt)
     mask = None if mask is None else np.ascontiguousarray(mask, dtype=np.float32)
     seg = None if seg is None else np.ascontiguousarray(seg, dtype=np.int32)
     k_lens = None if k_lens is None else np.ascontiguousarray(k_lens, dtype=np.int32)
@@ -149,6 +161,17 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
     if sink is not None and sink.shape != (p["heads"],):
         raise ValueError("head_sink must be float32 [heads]")
     prob.head_sink = None if sink is None else sink.ctypes.data
+    prob.kv_int8 = 1 if kv8 else 0
+    prob.kv_per_channel = 1 if p.get("kv_scale") == "channel" else 0
+    scales = []
+    if kv8:
+        n_sc = p["kv_heads"] * p["head_dim"] if prob.kv_per_channel else 1
+        for sc in (k_scale, v_scale):
+            sc = np.ascontiguousarray(sc, dtype=np.float32).reshape(-1)
+            if sc.size != n_sc:
+                raise ValueError(f"expected {n_sc} scales, got {sc.size}")
+            scales.append(sc)
+        prob.k_scale, prob.v_scale = scales[0].ctypes.data, scales[1].ctypes.data
     if rows is None:
         n_rows = p["batch"] * p["heads"] * p["q_len"]
         rows_arr = None

@@ -59,6 +59,13 @@
  *     LSE = sigma_h in both masked-rows modes; a NaN or +inf score (the sink
  *     included) still makes the row NaN, and a sink of -inf adds nothing.
  *
+ * Quantised key/value caches, from the same page (inputs k_scale and
+ * v_scale, attributes k_quant_type, v_quant_type and kv_cache_bit_width = 8):
+ * a cache element is a signed 8-bit integer and its value is that integer
+ * times a float32 scale -- one scale for the whole cache (PER_TENSOR) or one
+ * per (kv head, head-dim channel), kv_heads * head_dim of them (PER_CHANNEL).
+ * The product is exact in double.
+ *
  * Precision: every product and sum is in double.  Inputs are read in their
  * storage type (float32, IEEE half or bfloat16 bit patterns) and widened
  * exactly to double.  The combine routine follows "Attention", section
@@ -94,6 +101,10 @@ typedef struct {
   float softcap;          /* 0: off; > 0: scores are softcap * tanh(scale q.k / softcap) before the mask */
   int32_t smooth_softmax; /* 1: a sink logit joins each row's denominator (sigma = 0 unless head_sink) */
   const float* head_sink; /* NULL or float [heads]: per-head sink logits (turns the sink on) */
+  int32_t kv_int8;        /* 1: K and V are int8 with scales; Q keeps dtype */
+  int32_t kv_per_channel; /* 0: one scale each for K and V; 1: kv_heads * head_dim scales each */
+  const float* k_scale;
+  const float* v_scale;
 } orc_problem;
 
 /* ---- exact widening of the storage types --------------------------------- */
@@ -137,6 +148,14 @@ double orc_widen(int32_t dtype, uint32_t bits) {
     return (double)f;
   }
   return dtype == ORC_F16 ? orc_half_to_double((uint16_t)bits) : orc_bf16_to_double((uint16_t)bits);
+}
+
+/* One key or value element: the stored value, or int8 times its scale. */
+static double orc_load_kv(const orc_problem* p, const void* base, const float* scale, int64_t idx, int64_t g,
+                          int64_t d) {
+  if (!p->kv_int8) return orc_load(base, p->dtype, idx);
+  const double s = (double)scale[p->kv_per_channel ? g * p->head_dim + d : 0];
+  return (double)((const int8_t*)base)[idx] * s;
 }
 
 static int64_t orc_clamp(int64_t x, int64_t lo, int64_t hi) {
@@ -203,7 +222,7 @@ static void orc_row(const orc_job* j, int64_t b, int64_t h, int64_t qi,
     const int64_t kbase = p->k.offset + b * p->k.batch_stride + g * p->k.head_stride + kk * p->k.row_stride;
     double dot = 0.0;
     for (int64_t d = 0; d < D; ++d)
-      dot += orc_load(j->q, p->dtype, qbase + d) * orc_load(j->k, p->dtype, kbase + d);
+      dot += orc_load(j->q, p->dtype, qbase + d) * orc_load_kv(p, j->k, p->k_scale, kbase + d, g, d);
     double sc = scale * dot;
     if (p->softcap > 0.0f) {
       const double cap = (double)p->softcap;
@@ -255,7 +274,7 @@ static void orc_row(const orc_job* j, int64_t b, int64_t h, int64_t qi,
     if (!vis[kk] || !(s[kk] > -INFINITY)) continue;
     const double w = exp(s[kk] - m);
     const int64_t vbase = p->v.offset + b * p->v.batch_stride + g * p->v.head_stride + kk * p->v.row_stride;
-    for (int64_t d = 0; d < D; ++d) o_row[d] += w * orc_load(j->v, p->dtype, vbase + d);
+    for (int64_t d = 0; d < D; ++d) o_row[d] += w * orc_load_kv(p, j->v, p->v_scale, vbase + d, g, d);
   }
   for (int64_t d = 0; d < D; ++d) o_row[d] /= l;
   *lse_out = m + log(l);
