@@ -22,6 +22,8 @@ ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = 4, 5, 6
 ATTN_OFFSET_DEFAULT = -(2**63)
 ATTN_CAUSAL_FIXED, ATTN_CAUSAL_KLENS = 0, 1
 ATTN_KLENS_COUNT, ATTN_KLENS_LAST_INDEX = 0, 1
+ATTN_KV_AS_Q, ATTN_KV_INT8 = 0, 1
+ATTN_KV_SCALE_TENSOR, ATTN_KV_SCALE_CHANNEL = 0, 1
 DTYPE_CODE = {"f32": ATTN_F32, "f16": ATTN_F16, "bf16": ATTN_BF16}
 EXPORTS = ("attn_fwd_workspace_size", "attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_combine",
            "attn_device_status", "attn_status_string", "attn_version", "attn_decode_noalloc",
@@ -43,7 +45,9 @@ class attn_problem(ctypes.Structure):
                 ("lse_batch_stride", ctypes.c_int64), ("lse_head_stride", ctypes.c_int64),
                 ("window_left", ctypes.c_int32), ("causal_align", ctypes.c_int32),
                 ("k_lens_kind", ctypes.c_int32), ("softcap", ctypes.c_float),
-                ("smooth_softmax", ctypes.c_int32), ("head_sink", ctypes.c_void_p)]
+                ("smooth_softmax", ctypes.c_int32), ("head_sink", ctypes.c_void_p),
+                ("kv_dtype", ctypes.c_int32), ("kv_scale_kind", ctypes.c_int32),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):
@@ -163,6 +167,11 @@ def make_problem(d: dict) -> attn_problem:
     p.softcap = float(d.get("softcap") or 0.0)
     p.smooth_softmax = 1 if d.get("smooth_softmax") else 0
     p.head_sink = d.get("head_sink_ptr")      # device address of float32 [heads], or None
+    p.kv_dtype = ATTN_KV_INT8 if d.get("kv_dtype") in ("i8", ATTN_KV_INT8) else ATTN_KV_AS_Q
+    p.kv_scale_kind = (ATTN_KV_SCALE_CHANNEL if d.get("kv_scale") in ("channel", ATTN_KV_SCALE_CHANNEL)
+                       else ATTN_KV_SCALE_TENSOR)
+    p.k_scale = d.get("k_scale_ptr")          # device addresses of float32 scales (int8 caches)
+    p.v_scale = d.get("v_scale_ptr")
     return p
 
 
@@ -241,10 +250,12 @@ def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, 
 
 def decode(q, k_cache, v_cache, k_lens=None, *, scale=0.0, mask=None, masked_rows="nan", return_lse=False,
            out=None, lse=None, workspace=None, stream=None, window_left=None, k_lens_kind="count", softcap=0.0,
-           smooth_softmax=False, head_sink=None):
+           smooth_softmax=False, head_sink=None, k_scale=None, v_scale=None):
     """Single-query decode: q [B, 1, H, D]; caches BNSH [B, G, cap, D]; k_lens int32 [B].
     window_left keeps only the last window_left + 1 valid keys (local attention);
-    k_lens_kind 'last_index' takes ONNX seqlens_k (count minus one) as given."""
+    k_lens_kind 'last_index' takes ONNX seqlens_k (count minus one) as given.
+    int8 caches take float32 k_scale / v_scale tensors of 1 (per cache) or
+    G * D (per kv head and channel) elements."""
     torch = _torch()
     B, Sq, H, D = q.shape
     G, cap = k_cache.shape[1], k_cache.shape[2]
@@ -254,6 +265,9 @@ def decode(q, k_cache, v_cache, k_lens=None, *, scale=0.0, mask=None, masked_row
              causal=window_left is not None, causal_align="klens", window_left=window_left,
              k_lens_kind=k_lens_kind, softcap=softcap, smooth_softmax=smooth_softmax,
              head_sink_ptr=_ptr(head_sink), masked_rows=masked_rows, q_layout=_layout4(q, 2),
+             kv_dtype="i8" if k_cache.dtype == torch.int8 else None,
+             kv_scale="channel" if (k_scale is not None and k_scale.numel() > 1) else "tensor",
+             k_scale_ptr=_ptr(k_scale), v_scale_ptr=_ptr(v_scale),
              k_layout=_layout4(k_cache, 1), v_layout=_layout4(v_cache, 1), o_layout=_layout4(out, 2))
     if mask is not None:
         d["mask_layout"] = (0, mask.stride(0) if mask.shape[0] > 1 else 0,

@@ -66,6 +66,13 @@ int check_problem(const attn_problem* p) {
   if (!(p->softcap >= 0.0f) || isinf(p->softcap)) return ATTN_ERR_INVALID_ARG;
   if (p->smooth_softmax != 0 && p->smooth_softmax != 1) return ATTN_ERR_INVALID_ARG;
   if (p->head_sink && !aligned(p->head_sink, 4)) return ATTN_ERR_ALIGNMENT;
+  if (p->kv_dtype != ATTN_KV_AS_Q && p->kv_dtype != ATTN_KV_INT8) return ATTN_ERR_INVALID_ARG;
+  if (p->kv_scale_kind != ATTN_KV_SCALE_TENSOR && p->kv_scale_kind != ATTN_KV_SCALE_CHANNEL)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->kv_dtype == ATTN_KV_INT8) {
+    if (!p->k_scale || !p->v_scale) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)) return ATTN_ERR_ALIGNMENT;
+  }
   return ATTN_OK;
 }
 
@@ -91,6 +98,10 @@ Problem resolve(const attn_problem* p, const void* q, const void* k, const void*
   r.softcap = p->softcap;
   r.sink_on = (p->smooth_softmax || p->head_sink) ? 1 : 0;
   r.sink = p->head_sink;
+  r.kv_int8 = p->kv_dtype == ATTN_KV_INT8;
+  r.kv_per_channel = p->kv_scale_kind == ATTN_KV_SCALE_CHANNEL;
+  r.k_scale = p->k_scale;
+  r.v_scale = p->v_scale;
   r.q = {p->q.offset, p->q.batch_stride, p->q.head_stride, p->q.row_stride};
   r.k = {p->k.offset, p->k.batch_stride, p->k.head_stride, p->k.row_stride};
   r.v = {p->v.offset, p->v.batch_stride, p->v.head_stride, p->v.row_stride};
@@ -114,9 +125,10 @@ Problem resolve(const attn_problem* p, const void* q, const void* k, const void*
 int check_pointers(const attn_problem* p, const void* q, const void* k, const void* v, const void* o,
                    const float* mask, const int32_t* seg, const int32_t* k_lens, const float* lse) {
   const size_t es = elem_size(p->dtype);
+  const size_t kv_es = p->kv_dtype == ATTN_KV_INT8 ? 1 : es;
   if (!q || !o) return ATTN_ERR_INVALID_ARG;
   if (p->k_len > 0 && (!k || !v)) return ATTN_ERR_INVALID_ARG;
-  if (!aligned(q, es) || !aligned(o, es) || (k && !aligned(k, es)) || (v && !aligned(v, es)))
+  if (!aligned(q, es) || !aligned(o, es) || (k && !aligned(k, kv_es)) || (v && !aligned(v, kv_es)))
     return ATTN_ERR_ALIGNMENT;
   if ((mask && !aligned(mask, 4)) || (seg && !aligned(seg, 4)) || (k_lens && !aligned(k_lens, 4)) ||
       (lse && !aligned(lse, 4)))
@@ -215,7 +227,7 @@ int attn_decode(const attn_problem* p, const void* q, const void* k_cache, const
                                         round256(rows * n_splits * p->head_dim * sizeof(float)));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int used = 0;
-  rc = decode_fast_try(r, s, st, &used);
+  rc = r.kv_int8 ? decode_q8_try(r, s, st, &used) : decode_fast_try(r, s, st, &used);
   if (rc) return rc;
   if (!used) {
     rc = from_cuda(launch_simt(r, s, st));
@@ -264,6 +276,6 @@ const char* attn_status_string(int status) {
   }
 }
 
-int attn_version(void) { return 210; }
+int attn_version(void) { return 220; }
 
 }  // extern "C"

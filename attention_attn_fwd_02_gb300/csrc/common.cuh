@@ -30,6 +30,10 @@ struct Problem {
   float softcap;                 // 0: off; > 0: scores are softcap * tanh(scale q.k / softcap)
   int sink_on;                   // 1: a sink logit joins every row's denominator
   const float* sink;             // per-head sink logits (nullptr: 0 for every head)
+  int kv_int8;                   // 1: K and V are int8, value = integer * scale
+  int kv_per_channel;            // 1: scales per (kv head, channel); 0: one scale each
+  const float* k_scale;
+  const float* v_scale;
   Layout q, k, v, o, m;
   int64_t seg_bs, lse_bs, lse_hs;
   const void* Q;

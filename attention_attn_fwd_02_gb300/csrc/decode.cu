@@ -444,6 +444,7 @@ namespace attn {
 int decode_fast_try(const Problem& p, const Split& s, cudaStream_t st, int* used) {
   *used = 0;
   if (p.dtype != ATTN_BF16 && p.dtype != ATTN_F16) return ATTN_OK;
+  if (p.kv_int8) return ATTN_OK;
   if (p.D != dec::kD || p.Sq != 1 || s.n_splits < 1) return ATTN_OK;
   if (!tma_layout_ok(p.K, p.k, p.Sk, p.G, p.B) || !tma_layout_ok(p.V, p.v, p.Sk, p.G, p.B)) return ATTN_OK;
   const int rc = p.dtype == ATTN_BF16 ? dec::launch_mma<true>(p, s, st) : dec::launch_mma<false>(p, s, st);

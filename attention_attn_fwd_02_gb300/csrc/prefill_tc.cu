@@ -520,6 +520,7 @@ int launch_d(const Problem& p, cudaStream_t st) {
 int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
   *used = 0;
   if (p.dtype != ATTN_BF16 && p.dtype != ATTN_F16) return ATTN_OK;
+  if (p.kv_int8) return ATTN_OK;  // int8 caches: the CUDA-core path
   if (p.D != 64 && p.D != 128 && p.D != 256) return ATTN_OK;
   if (p.Sk < 1 || p.Sq < 1) return ATTN_OK;
   if (p.Sk > 0x3fffffff || p.Sq > 0x3fffffff) return ATTN_OK;

@@ -32,7 +32,8 @@ constexpr int kThreads = 128;
 constexpr int kSlots = 8;    // head_dim elements per thread
 constexpr int kTile = 32;    // keys per staged tile
 
-template <typename T, int TPR>
+// KV8: K and V are int8 (value = integer * scale) instead of T.
+template <typename T, int TPR, bool KV8>
 __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp, int64_t row_blocks) {
   constexpr int RPC = kThreads / TPR;  // rows per CTA
   extern __shared__ float smem[];
@@ -101,8 +102,14 @@ __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp
       const int kk = t0 + j;
       float kv = 0.f, vv = 0.f;
       if (kk >= u_lo && kk < u_hi) {
-        kv = to_f32(K[kb + (int64_t)kk * p.k.rs + d]);
-        vv = to_f32(V[vb + (int64_t)kk * p.v.rs + d]);
+        if constexpr (KV8) {
+          const int si = p.kv_per_channel ? g * D + d : 0;
+          kv = (float)reinterpret_cast<const int8_t*>(p.K)[kb + (int64_t)kk * p.k.rs + d] * p.k_scale[si];
+          vv = (float)reinterpret_cast<const int8_t*>(p.V)[vb + (int64_t)kk * p.v.rs + d] * p.v_scale[si];
+        } else {
+          kv = to_f32(K[kb + (int64_t)kk * p.k.rs + d]);
+          vv = to_f32(V[vb + (int64_t)kk * p.v.rs + d]);
+        }
       }
       Ks[e] = kv;
       Vs[e] = vv;
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(128) combine_kernel(int n_splits, int64_t rows
         bad ? NAN : (M == -INFINITY ? -INFINITY : M + logf(ws));
 }
 
-template <typename T, int TPR>
+template <typename T, int TPR, bool KV8>
 cudaError_t launch_simt_t(const Problem& p, const Split& s, cudaStream_t st) {
   constexpr int RPC = kThreads / TPR;
   const int64_t rows = (int64_t)p.Sq * p.qpg;
@@ -253,18 +260,23 @@ cudaError_t launch_simt_t(const Problem& p, const Split& s, cudaStream_t st) {
   if (blocks <= 0) return cudaSuccess;
   if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)2 * kTile * p.D * sizeof(float);
-  cudaError_t e = ensure_smem((const void*)simt_attn_kernel<T, TPR>, (int)smem);
+  cudaError_t e = ensure_smem((const void*)simt_attn_kernel<T, TPR, KV8>, (int)smem);
   if (e != cudaSuccess) return e;
-  simt_attn_kernel<T, TPR><<<(unsigned)blocks, kThreads, smem, st>>>(p, s, row_blocks);
+  simt_attn_kernel<T, TPR, KV8><<<(unsigned)blocks, kThreads, smem, st>>>(p, s, row_blocks);
   return cudaGetLastError();
+}
+
+template <typename T, bool KV8>
+cudaError_t launch_simt_k(const Problem& p, const Split& s, cudaStream_t st) {
+  if (p.D <= 32) return launch_simt_t<T, 4, KV8>(p, s, st);
+  if (p.D <= 64) return launch_simt_t<T, 8, KV8>(p, s, st);
+  if (p.D <= 128) return launch_simt_t<T, 16, KV8>(p, s, st);
+  return launch_simt_t<T, 32, KV8>(p, s, st);
 }
 
 template <typename T>
 cudaError_t launch_simt_d(const Problem& p, const Split& s, cudaStream_t st) {
-  if (p.D <= 32) return launch_simt_t<T, 4>(p, s, st);
-  if (p.D <= 64) return launch_simt_t<T, 8>(p, s, st);
-  if (p.D <= 128) return launch_simt_t<T, 16>(p, s, st);
-  return launch_simt_t<T, 32>(p, s, st);
+  return p.kv_int8 ? launch_simt_k<T, true>(p, s, st) : launch_simt_k<T, false>(p, s, st);
 }
 
 template <typename T>

@@ -100,6 +100,8 @@ class Case:
     seg: np.ndarray | None = None
     k_lens: np.ndarray | None = None
     head_sink: np.ndarray | None = None
+    k_scale: np.ndarray | None = None
+    v_scale: np.ndarray | None = None
     decode: bool = False
     meta: dict = field(default_factory=dict)
 
@@ -122,12 +124,15 @@ def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, head
               masked_rows="nan", value_scale=1.0, k_lens=None, seg=None, mask=None,
               mask_kind="b11k", nan_fill=True, packed=False, decode=False, window_left=None,
               causal_align="fixed", k_lens_kind="count", softcap=0.0, smooth_softmax=False,
-              head_sink=None) -> Case:
+              head_sink=None, kv_dtype=None, kv_scale="channel") -> Case:
     """A general seeded problem.
 
     k_lens / seg / mask may be arrays (used as given) or None.  window_left,
     causal_align and k_lens_kind are the visibility variants of the problem
-    (k_lens holds the values as passed: count - 1 under 'last_index').  mask_kind names
+    (k_lens holds the values as passed: count - 1 under 'last_index').
+    kv_dtype='i8' stores K and V as int8 (uniform in [-127, 127]; rows beyond a
+    batch entry's length are -128) with float32 scales per (kv head, channel)
+    ('channel', uniform in [0.005, 0.02]) or one per cache ('tensor').  mask_kind names
     the broadcast shape of a given mask: 'b11k' [B,1,1,K], 'bhqk' [B,H,Q,K],
     '11qk' [1,1,Q,K].  packed=True stores Q, K and V as slices of one
     [B, S, H + 2*KVH, D] projection (q_len must equal k_len).  decode=True
@@ -198,8 +203,28 @@ def make_case(*, name="case", seed=0, dtype="bf16", layout="bshd", batch=1, head
     prob["lse_layout"] = (H * Sq, Sq)   # LSE [B, H, q_len] float32
     if head_sink is not None:
         head_sink = np.ascontiguousarray(head_sink, dtype=np.float32)
+    k_scale = v_scale = None
+    if kv_dtype == "i8":
+        assert not packed
+        r8 = rng(seed, K_ID + 10)
+        k = r8.integers(-127, 128, size=kshape, dtype=np.int8)
+        v = r8.integers(-127, 128, size=vshape, dtype=np.int8)
+        if k_lens is not None and nan_fill:
+            for b in range(B):
+                kl = int(min(max(int(k_lens[b]) + (1 if k_lens_kind == "last_index" else 0), 0), Sk))
+                if kv_kind == "bshd":
+                    k[b, kl:] = -128
+                    v[b, kl:] = -128
+                else:
+                    k[b, :, kl:] = -128
+                    v[b, :, kl:] = -128
+        n_sc = G * D if kv_scale == "channel" else 1
+        k_scale = r8.uniform(0.005, 0.02, size=n_sc).astype(np.float32)
+        v_scale = r8.uniform(0.005, 0.02, size=n_sc).astype(np.float32)
+        prob["kv_dtype"] = "i8"
+        prob["kv_scale"] = kv_scale
     return Case(name=name, problem=prob, q=q, k=k, v=v, o_shape=o_shape, mask=mask, seg=seg,
-                k_lens=k_lens, head_sink=head_sink, decode=decode)
+                k_lens=k_lens, head_sink=head_sink, k_scale=k_scale, v_scale=v_scale, decode=decode)
 
 
 # ---- the five named workloads -------------------------------------------------

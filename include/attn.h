@@ -39,6 +39,14 @@
  * key gives O = 0 and LSE = sigma_h; a NaN or +inf sink makes the row NaN; a
  * sink of -inf adds nothing.
  *
+ * Quantised key/value cache ("com.microsoft.GroupQueryAttention", inputs
+ * k_scale and v_scale, attributes k_quant_type, v_quant_type and
+ * kv_cache_bit_width = 8).  With kv_dtype = ATTN_KV_INT8 the K and V elements
+ * are signed 8-bit integers (layouts in elements = bytes) and an element's
+ * value is the integer times its float32 scale: k_scale[0] for every element
+ * (ATTN_KV_SCALE_TENSOR) or k_scale[g * head_dim + d] for kv head g, channel d
+ * (ATTN_KV_SCALE_CHANNEL); likewise v_scale.  Q and O keep dtype.
+ *
  * Memory.  Every data pointer is a DEVICE pointer owned by the caller.  The
  * library allocates no device memory: scratch space is the caller's
  * `workspace` (size from the *_workspace_size queries).  K/V values of keys
@@ -86,7 +94,7 @@ enum {
   ATTN_ERR_INVALID_ARG = 1,    /* null required pointer, negative size, heads % kv_heads != 0,
                                   head_dim outside [1, 256], odd head_dim for f16/bf16, bad layout,
                                   window_left < -1 or a window without causal, unknown enum value,
-                                  negative or non-finite softcap */
+                                  negative or non-finite softcap, int8 K/V without scales */
   ATTN_ERR_UNSUPPORTED = 2,    /* a valid combination this build does not implement */
   ATTN_ERR_ALIGNMENT = 3,      /* a pointer not aligned to its element size */
   ATTN_ERR_WORKSPACE = 4,      /* workspace missing or smaller than the size query says */
@@ -109,6 +117,10 @@ enum { ATTN_CAUSAL_FIXED = 0, ATTN_CAUSAL_KLENS = 1 };
  * ATTN_KLENS_COUNT: the number of valid keys; ATTN_KLENS_LAST_INDEX: the index
  * of the last valid key, i.e. the count minus one (ONNX seqlens_k as given). */
 enum { ATTN_KLENS_COUNT = 0, ATTN_KLENS_LAST_INDEX = 1 };
+
+/* Storage of K and V (see "Quantised key/value cache" above). */
+enum { ATTN_KV_AS_Q = 0, ATTN_KV_INT8 = 1 };
+enum { ATTN_KV_SCALE_TENSOR = 0, ATTN_KV_SCALE_CHANNEL = 1 };
 
 /* A strided 4-D view [batch][head][row][element]: element (b, h, r, e) is at
  * base[offset + b*batch_stride + h*head_stride + r*row_stride + e].  Strides
@@ -147,6 +159,11 @@ typedef struct {
   int32_t smooth_softmax;          /* 1: the sink term is on, sigma_h = 0 unless head_sink is given */
   const float* head_sink;          /* nullable DEVICE pointer, float32 [heads]: per-head sink logits;
                                       non-NULL turns the sink term on.  Owned by the caller. */
+  /* Key/value storage (see above). */
+  int32_t kv_dtype;                /* ATTN_KV_AS_Q / ATTN_KV_INT8 */
+  int32_t kv_scale_kind;           /* ATTN_KV_SCALE_TENSOR / ATTN_KV_SCALE_CHANNEL */
+  const float* k_scale;            /* DEVICE float32 scales, required with ATTN_KV_INT8 */
+  const float* v_scale;
 } attn_problem;
 
 /* Bytes of device workspace attn_fwd needs for this problem (0 when none).

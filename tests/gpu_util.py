@@ -67,7 +67,10 @@ class GpuCase:
         self.lse_buf = torch.full((B * H * Sq + 2 * guard,), 777.0, dtype=torch.float32, device="cuda") if lse else None
         self.lse = self.lse_buf[guard:guard + B * H * Sq] if lse else None
         self.sink = dev(case.head_sink)
-        self.prob = attn.make_problem(dict(p, head_sink_ptr=None if self.sink is None else self.sink.data_ptr()))
+        self.k_scale, self.v_scale = dev(case.k_scale), dev(case.v_scale)
+        ptr = (lambda t: None if t is None else t.data_ptr())
+        self.prob = attn.make_problem(dict(p, head_sink_ptr=ptr(self.sink), k_scale_ptr=ptr(self.k_scale),
+                                           v_scale_ptr=ptr(self.v_scale)))
         self.ws = None
         self.ws_bytes = 0
 
@@ -122,7 +125,7 @@ class GpuCase:
 def oracle_full(case: wl.Case):
     p = case.problem
     o, lse = oracle.attn(p, case.q, case.k, case.v, mask=case.mask, seg=case.seg, k_lens=case.k_lens,
-                         head_sink=case.head_sink)
+                         head_sink=case.head_sink, k_scale=case.k_scale, v_scale=case.v_scale)
     B, H, Sq, D = p["batch"], p["heads"], p["q_len"], p["head_dim"]
     return o.reshape(B, H, Sq, D), lse.reshape(B, H, Sq)
 

@@ -49,14 +49,15 @@ def test_struct_layout_matches_c(tmp_path):
                    ' offsetof(attn_problem, lse_head_stride)); printf("%zu %zu %zu\\n",'
                    ' offsetof(attn_problem, window_left), offsetof(attn_problem, causal_align),'
                    ' offsetof(attn_problem, k_lens_kind)); printf("%zu %zu\\n", offsetof(attn_problem, softcap),'
-                   ' offsetof(attn_problem, head_sink)); return 0;}\n')
+                   ' offsetof(attn_problem, head_sink)); printf("%zu %zu\\n", offsetof(attn_problem, kv_dtype),'
+                   ' offsetof(attn_problem, v_scale)); return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.run(["gcc", str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     P = attn.attn_problem
     want = [ctypes.sizeof(P), P.causal_offset.offset, P.q.offset, P.mask.offset, P.seg_batch_stride.offset,
             P.lse_head_stride.offset, P.window_left.offset, P.causal_align.offset, P.k_lens_kind.offset,
-            P.softcap.offset, P.head_sink.offset]
+            P.softcap.offset, P.head_sink.offset, P.kv_dtype.offset, P.v_scale.offset]
     assert got == want
 
 
@@ -91,6 +92,9 @@ FAKE = 0x10000  # never dereferenced: every case below fails on the host first
     (dict(softcap=float("inf")), attn.ATTN_ERR_INVALID_ARG),
     (dict(smooth_softmax=2), attn.ATTN_ERR_INVALID_ARG),
     (dict(head_sink_ptr=FAKE + 2), attn.ATTN_ERR_ALIGNMENT),
+    (dict(kv_dtype="i8"), attn.ATTN_ERR_INVALID_ARG),              # int8 K/V need their scales
+    (dict(kv_dtype="i8", k_scale_ptr=FAKE, v_scale_ptr=FAKE + 1), attn.ATTN_ERR_ALIGNMENT),
+    (dict(kv_dtype=5), attn.ATTN_ERR_INVALID_ARG),
 ])
 def test_fwd_rejects_invalid_problems(L, kw, code):
     p = base_problem(**kw)
@@ -98,8 +102,8 @@ def test_fwd_rejects_invalid_problems(L, kw, code):
         p.causal = int(kw["causal"])
     if "masked_rows" in kw:
         p.masked_rows = kw["masked_rows"]
-    for name in ("causal_align", "k_lens_kind", "smooth_softmax"):
-        if name in kw:
+    for name in ("causal_align", "k_lens_kind", "smooth_softmax", "kv_dtype"):
+        if isinstance(kw.get(name), int):
             setattr(p, name, kw[name])
     assert attn.attn_fwd(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None, 0, None) == code
 
@@ -145,4 +149,4 @@ def test_status_strings_and_version(L):
     for code in range(7):
         assert attn.status_string(code) and attn.status_string(code) != "unknown status"
     assert attn.status_string(99) == "unknown status"
-    assert attn.attn_version() >= 210
+    assert attn.attn_version() >= 220

@@ -395,3 +395,41 @@ def test_decode_single_range_generic_pass():
     c = wl.make_case(name="dec1r", seed=977, dtype="f16", batch=3, heads=4, kv_heads=2, q_len=1, k_len=96,
                      head_dim=64, k_lens=np.array([96, 1, 50], dtype=np.int32), decode=True)
     run_and_compare(c)
+
+
+# ---- int8 key/value caches ------------------------------------------------------------------------
+
+INT8 = [
+    # dtype, B, H, G, cap, D, scale kind, mask, extras
+    ("bf16", 4, 32, 8, 3000, 128, "channel", False, {}),                                   # tensor-core pass
+    ("f16", 3, 16, 16, 1500, 128, "tensor", True, {}),                                     # one head per group
+    ("bf16", 2, 40, 2, 2100, 128, "channel", False, dict(softcap=2.0, head_sink="heads",
+                                                          window_left=700)),               # with transforms
+    ("bf16", 2, 8, 2, 900, 64, "channel", True, {}),                                       # generic pass
+]
+
+
+@pytest.mark.parametrize("i", range(len(INT8)))
+def test_decode_int8_cache(i):
+    dtype, B, H, G, cap, D, kind, use_mask, extra = INT8[i]
+    r = np.random.default_rng(1100 + i)
+    k_lens = r.integers(1, cap + 1, size=B).astype(np.int32)
+    mask = None
+    if use_mask:
+        mask = r.standard_normal((B, 1, 1, cap)).astype(np.float32)
+        mask[r.random(mask.shape) < 0.15] = -np.inf
+    extra = dict(extra)
+    if extra.get("head_sink") == "heads":
+        extra["head_sink"] = (r.standard_normal(H) * 2).astype(np.float32)
+    if "window_left" in extra:
+        extra.update(causal=True, causal_align="klens")
+    c = wl.make_case(name=f"q8_{i}", seed=1200 + i, dtype=dtype, batch=B, heads=H, kv_heads=G, q_len=1, k_len=cap,
+                     head_dim=D, k_lens=k_lens, mask=mask, decode=True, kv_dtype="i8", kv_scale=kind, **extra)
+    run_and_compare(c)
+
+
+def test_prefill_int8_cache_generic_path():
+    c = wl.make_case(name="q8_prefill", seed=1300, dtype="bf16", layout="bhsd", batch=2, heads=4, kv_heads=2,
+                     q_len=70, k_len=150, head_dim=64, causal=True, k_lens=np.array([150, 90], dtype=np.int32),
+                     kv_dtype="i8", kv_scale="channel")
+    run_and_compare(c)
