@@ -142,8 +142,24 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA
 // of 32 keys, at least 128 keys, at most 16 of them ("Attention", section
 // "Accuracy at long key lengths"); a range of 512 keys or more is kept
 // whole when the (batch, kv head) pairs alone fill the GPU several times.
+//
+// int8 caches carry half the bytes per key, so a range's fixed costs (Q
+// load and scaling, the four-warp merge, the partial write) weigh twice as
+// much: their plan targets about 2048 ranges in all over (batch, kv head)
+// pairs, at most 16 a row, each a multiple of the 64-key stage.
 void decode_plan(const attn_problem* p, int* n_splits, int* split_len) {
   const int64_t Sk = p->k_len > 0 ? p->k_len : 1;
+  if (p->kv_dtype == ATTN_KV_INT8) {
+    const int64_t pairs = (int64_t)(p->batch > 0 ? p->batch : 1) * p->kv_heads;
+    int64_t n = (2048 + pairs - 1) / pairs;
+    n = n < 1 ? 1 : (n > 16 ? 16 : n);
+    int64_t len = (Sk + n - 1) / n;
+    len = (len + 63) / 64 * 64;
+    if (len < 128) len = 128;
+    *split_len = (int)len;
+    *n_splits = (int)((Sk + len - 1) / len);
+    return;
+  }
   int64_t len = (Sk + 15) / 16;
   len = (len + 31) / 32 * 32;
   if (len < 128) len = 128;

@@ -32,9 +32,10 @@
 //
 // CTA: 4 warps; one (batch, kv head, key range) and up to 16 query heads of
 // that kv head (the MMA rows), so each cache byte is read once.  The range
-// streams through shared memory in 64-key stages, six deep, copied by TMA
-// with 128-byte swizzle (conflict-free 32-bit reads); warp w takes keys
-// 16w .. 16w+15 of a stage.  Waits are bounded (status word on timeout).
+// streams through shared memory in 64-key stages, three deep (48 KB, so four
+// CTAs share an SM), copied by TMA with 128-byte swizzle (conflict-free
+// 32-bit reads); warp w takes keys 16w .. 16w+15 of a stage.  Waits are
+// bounded (status word on timeout).
 #include <stdlib.h>
 
 #include <type_traits>
@@ -58,7 +59,7 @@ constexpr int kD = 128;
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStageKeys = 64;
-constexpr int kStages = 6;
+constexpr int kStages = 3;
 constexpr int kTile = kStageKeys * kD;   // bytes of the K (or V) tile of a stage
 constexpr int kHeads = 16;               // query heads per CTA (MMA rows)
 constexpr float kLog2e = 1.4426950408889634f;

@@ -265,6 +265,17 @@ def decode_bnsh_bf16(seed: int = 4, batch: int = 64, capacity: int = 8192, heads
                      head_dim=128, k_lens=k_lens, decode=True)
 
 
+def decode_bnsh_int8(seed: int = 4, batch: int = 64, capacity: int = 8192, heads: int = 32,
+                     kv_heads: int = 8, min_len: int = 512) -> Case:
+    """The batched decode workload with an int8 BNSH cache and per-(kv head, channel) scales
+    (bf16 queries): the same lengths as decode_bnsh_bf16, half the cache bytes."""
+    r = rng(seed, LEN_ID)
+    k_lens = r.integers(min_len, capacity + 1, size=batch).astype(np.int32)
+    return make_case(name=f"decode_bnsh_int8_b{batch}_h{heads}_kv{kv_heads}_cap{capacity}_d128", seed=seed,
+                     dtype="bf16", batch=batch, heads=heads, kv_heads=kv_heads, q_len=1, k_len=capacity,
+                     head_dim=128, k_lens=k_lens, decode=True, kv_dtype="i8", kv_scale="channel")
+
+
 def cross_mask_f16(seed: int = 5, batch: int = 8, q_len: int = 512, k_len: int = 2048, heads: int = 16,
                    masked_rows: str = "nan") -> Case:
     """fp16 cross-attention, head dim 256, additive float32 mask [B,1,1,K]: N(0,1), 10% of keys -inf,

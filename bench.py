@@ -79,9 +79,11 @@ def job_throughput(units_per_rank: float, world: int, steps: int, slowest_second
 
 
 def decode_kv_bytes(case) -> int:
+    """K and V bytes of the valid cache rows (2 bytes an element, 1 for an int8 cache)."""
     p = case.problem
     kl = np.clip(case.k_lens.astype(np.int64), 0, p["k_len"])
-    return int(kl.sum()) * p["kv_heads"] * p["head_dim"] * 2 * 2   # K and V, bf16
+    es = 1 if p.get("kv_dtype") == "i8" else 2
+    return int(kl.sum()) * p["kv_heads"] * p["head_dim"] * 2 * es
 
 
 def source_digest(*names) -> str:
@@ -450,6 +452,7 @@ CASES = {
     "gqa_doc_causal_bf16": lambda: wl.gqa_doc_causal_bf16(),
     "long_causal_gqa_bf16": lambda: wl.long_causal_gqa_bf16(),
     "decode_bnsh_bf16": lambda: wl.decode_bnsh_bf16(),
+    "decode_bnsh_int8": lambda: wl.decode_bnsh_int8(),
     "cross_mask_f16": lambda: wl.cross_mask_f16(),
     "cross_mask_f16_zero": lambda: wl.cross_mask_f16(masked_rows="zero"),
 }
