@@ -77,6 +77,10 @@ def _load():
         lib.orc_combine.restype = ctypes.c_int
         lib.orc_combine.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+        lib.orc_append_rows.restype = ctypes.c_int
+        lib.orc_append_rows.argtypes = ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] +
+                                        [ctypes.c_int32] * 5 + [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32])
         lib.orc_widen.restype = ctypes.c_double
         lib.orc_widen.argtypes = [ctypes.c_int32, ctypes.c_uint32]
         lib.orc_default_scale.restype = ctypes.c_float
@@ -186,6 +190,35 @@ def attn(problem: dict, q, k, v, mask=None, seg=None, k_lens=None, rows=None, nt
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (status {rc})")
     return o, lse
+
+
+def append_rows(problem: dict, k_cache, v_cache, k_new, v_new, k_lens, k_scale=None, v_scale=None):
+    """The cache update before a decode step: copies of the BNSH caches with each
+    (batch, kv head)'s new row written at position L_b - 1 (see attn_oracle.c).
+    k_new / v_new: [batch, kv_heads, head_dim] storage of the problem's dtype;
+    caches: storage of the problem's dtype, or int8 when problem['kv_dtype'] == 'i8'.
+    Returns (k_cache', v_cache')."""
+    lib = _load()
+    p = problem
+    B, G, D, cap = p["batch"], p["kv_heads"], p["head_dim"], p["k_len"]
+    kv8 = p.get("kv_dtype") == "i8"
+    per_ch = 1 if p.get("kv_scale") == "channel" else 0
+    plus = 1 if p.get("k_lens_kind") in ("last_index", 1) else 0
+    k_lens = np.ascontiguousarray(k_lens, dtype=np.int32)
+    out = []
+    for cache, new, sc in ((k_cache, k_new, k_scale), (v_cache, v_new, v_scale)):
+        c = np.array(cache, copy=True, order="C")
+        n = _storage(np.ascontiguousarray(new), p["dtype"])
+        lay = p["k_layout"]
+        elem = 1 if kv8 else (4 if p["dtype"] == "f32" else 2)
+        scale = None if sc is None else np.ascontiguousarray(sc, dtype=np.float32).reshape(-1)
+        rc = lib.orc_append_rows(c.ctypes.data + lay[0] * elem, lay[1], lay[2], lay[3], cap, B, G, D, elem,
+                                 n.ctypes.data, DTYPES[p["dtype"]], k_lens.ctypes.data, plus,
+                                 None if scale is None else scale.ctypes.data, per_ch)
+        if rc != 0:
+            raise ValueError("oracle append rejected its arguments")
+        out.append(c)
+    return out[0], out[1]
 
 
 def combine(part_o, part_lse, masked_rows="nan"):

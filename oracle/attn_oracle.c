@@ -66,6 +66,16 @@
  * per (kv head, head-dim channel), kv_heads * head_dim of them (PER_CHANNEL).
  * The product is exact in double.
  *
+ * Cache append ("com.microsoft.GroupQueryAttention": present_key /
+ * present_value with past and present sharing one buffer; seqlens_k is the
+ * total length including the new token; the int8 decode variant appends
+ * int8-quantised rows): orc_append_rows writes each (batch, kv head)'s new
+ * row at cache position L_b - 1, L_b the clamped length; nothing when
+ * L_b = 0.  Reading for int8 caches (the pages give no rounding rule): the
+ * code is x / scale rounded to the nearest integer, ties to even, saturated
+ * to [-128, 127], computed in float32 -- the precision of the kernel that
+ * takes the same decision.
+ *
  * Precision: every product and sum is in double.  Inputs are read in their
  * storage type (float32, IEEE half or bfloat16 bit patterns) and widened
  * exactly to double.  The combine routine follows "Attention", section
@@ -354,6 +364,45 @@ int orc_attn_rows(const orc_problem* p, const void* q, const void* k, const void
     if (jobs[t].status) status = jobs[t].status;
   }
   return status;
+}
+
+/*
+ * orc_append_rows: the cache update that precedes a decode step.  For each
+ * batch entry b with L_b = clamp(k_lens[b] + plus, 0, cap) >= 1 and each kv
+ * head g, row L_b - 1 of the cache (BNSH: cache + b*bs + g*hs + row*rs) takes
+ * new[(b * kv_heads + g) * D .. + D).  elem: 2 or 4 bytes when the cache holds
+ * the new rows' type (a bit copy); 1 for an int8 cache, whose codes are the
+ * float32-rounded x / scale (see the header), the new rows then being of
+ * new_dtype (ORC_F32 / ORC_F16 / ORC_BF16) with scales per tensor (n_scale 1)
+ * or per (g, d).  Returns 0, or -1 on a bad argument.
+ */
+int orc_append_rows(void* cache, int64_t bs, int64_t hs, int64_t rs, int32_t cap, int32_t batch,
+                    int32_t kv_heads, int32_t D, int32_t elem, const void* new_rows, int32_t new_dtype,
+                    const int32_t* k_lens, int32_t plus, const float* scale, int32_t per_channel) {
+  if (!cache || !new_rows || !k_lens || cap < 0 || batch < 0 || kv_heads < 1 || D < 1) return -1;
+  if (elem != 1 && elem != 2 && elem != 4) return -1;
+  if (elem == 1 && !scale) return -1;
+  for (int64_t b = 0; b < batch; ++b) {
+    const int64_t L = orc_clamp((int64_t)k_lens[b] + plus, 0, cap);
+    if (L < 1) continue;
+    for (int64_t g = 0; g < kv_heads; ++g) {
+      const int64_t src = (b * kv_heads + g) * D;
+      const int64_t dst = b * bs + g * hs + (L - 1) * rs;
+      if (elem == 1) {
+        for (int64_t d = 0; d < D; ++d) {
+          const float x = (float)orc_load(new_rows, new_dtype, src + d);
+          const float s = scale[per_channel ? g * D + d : 0];
+          float c = rintf(x / s);                       /* float32 division, ties to even */
+          if (c > 127.0f) c = 127.0f;
+          if (c < -128.0f) c = -128.0f;
+          ((int8_t*)cache)[dst + d] = (int8_t)c;
+        }
+      } else {
+        memcpy((char*)cache + dst * elem, (const char*)new_rows + src * elem, (size_t)D * elem);
+      }
+    }
+  }
+  return 0;
 }
 
 /*
