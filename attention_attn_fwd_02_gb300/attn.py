@@ -27,7 +27,7 @@ ATTN_KV_SCALE_TENSOR, ATTN_KV_SCALE_CHANNEL = 0, 1
 DTYPE_CODE = {"f32": ATTN_F32, "f16": ATTN_F16, "bf16": ATTN_BF16}
 EXPORTS = ("attn_fwd_workspace_size", "attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_combine",
            "attn_device_status", "attn_status_string", "attn_version", "attn_decode_noalloc",
-           "attn_decode_noalloc_max_scratch")
+           "attn_decode_noalloc_max_scratch", "attn_decode_append")
 
 
 class attn_layout(ctypes.Structure):
@@ -83,6 +83,8 @@ def lib():
         L.attn_decode_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.attn_decode_noalloc.restype = ctypes.c_int
         L.attn_decode_noalloc_max_scratch.argtypes, L.attn_decode_noalloc_max_scratch.restype = [], sz
+        L.attn_decode_append.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.attn_decode_append.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -111,6 +113,12 @@ def attn_decode_noalloc(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse, strea
     """attn_decode with the library's fixed device scratch array instead of a caller workspace,
     for callers that cannot allocate device memory (see include/attn.h)."""
     return lib().attn_decode_noalloc(ctypes.byref(p), q, k_cache, v_cache, o, mask, seg, k_lens, lse, stream)
+
+
+def attn_decode_append(p, q, k_new, v_new, k_cache, v_cache, o, mask, k_lens, lse, workspace, workspace_bytes,
+                       stream) -> int:
+    return lib().attn_decode_append(ctypes.byref(p), q, k_new, v_new, k_cache, v_cache, o, mask, k_lens, lse,
+                                    workspace, workspace_bytes, stream)
 
 
 def attn_decode_noalloc_max_scratch() -> int:

@@ -178,6 +178,48 @@ size_t decode_ws_bytes(const attn_problem* p, int n_splits) {
 }  // namespace
 }  // namespace attn
 
+namespace attn {
+namespace {
+int decode_impl(const attn_problem* p, const void* q, const void* k_cache, const void* v_cache, void* o,
+                const float* mask, const int32_t* seg, const int32_t* k_lens, float* lse, void* workspace,
+                size_t workspace_bytes, attn_stream stream, const void* k_new, const void* v_new) {
+  int rc = check_problem(p);
+  if (rc) return rc;
+  if (p->q_len != 1) return ATTN_ERR_INVALID_ARG;
+  if (p->batch == 0) return ATTN_OK;
+  rc = check_pointers(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse);
+  if (rc) return rc;
+  int n_splits = 1, split_len = 1;
+  decode_plan(p, &n_splits, &split_len);
+  const size_t need = decode_ws_bytes(p, n_splits);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return ATTN_ERR_ALIGNMENT;
+  int* status = nullptr;
+  rc = status_ptr(&status);
+  if (rc) return rc;
+  Problem r = resolve(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse, status);
+  r.k_new = k_new;
+  r.v_new = v_new;
+  const size_t rows = (size_t)p->batch * p->heads;
+  Split s;
+  s.n_splits = n_splits;
+  s.split_len = split_len;
+  s.part_o = static_cast<float*>(workspace);
+  s.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        round256(rows * n_splits * p->head_dim * sizeof(float)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int used = 0;
+  rc = r.kv_int8 ? decode_q8_try(r, s, st, &used) : decode_fast_try(r, s, st, &used);
+  if (rc) return rc;
+  if (!used) {
+    rc = from_cuda(launch_simt(r, s, st));
+    if (rc) return rc;
+  }
+  return from_cuda(launch_combine(r, s, p->dtype, st));
+}
+}  // namespace
+}  // namespace attn
+
 using namespace attn;
 
 extern "C" {
@@ -216,40 +258,25 @@ size_t attn_decode_workspace_size(const attn_problem* p) {
   return decode_ws_bytes(p, n);
 }
 
+
 int attn_decode(const attn_problem* p, const void* q, const void* k_cache, const void* v_cache, void* o,
                 const float* mask, const int32_t* seg, const int32_t* k_lens, float* lse, void* workspace,
                 size_t workspace_bytes, attn_stream stream) {
+  return attn::decode_impl(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse, workspace, workspace_bytes, stream,
+                           nullptr, nullptr);
+}
+
+int attn_decode_append(const attn_problem* p, const void* q, const void* k_new, const void* v_new,
+                       void* k_cache, void* v_cache, void* o, const float* mask, const int32_t* k_lens, float* lse,
+                       void* workspace, size_t workspace_bytes, attn_stream stream) {
   int rc = check_problem(p);
   if (rc) return rc;
-  if (p->q_len != 1) return ATTN_ERR_INVALID_ARG;
-  if (p->batch == 0) return ATTN_OK;
-  rc = check_pointers(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse);
-  if (rc) return rc;
-  int n_splits = 1, split_len = 1;
-  decode_plan(p, &n_splits, &split_len);
-  const size_t need = decode_ws_bytes(p, n_splits);
-  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return ATTN_ERR_ALIGNMENT;
-  int* status = nullptr;
-  rc = status_ptr(&status);
-  if (rc) return rc;
-  Problem r = resolve(p, q, k_cache, v_cache, o, mask, seg, k_lens, lse, status);
-  const size_t rows = (size_t)p->batch * p->heads;
-  Split s;
-  s.n_splits = n_splits;
-  s.split_len = split_len;
-  s.part_o = static_cast<float*>(workspace);
-  s.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        round256(rows * n_splits * p->head_dim * sizeof(float)));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int used = 0;
-  rc = r.kv_int8 ? decode_q8_try(r, s, st, &used) : decode_fast_try(r, s, st, &used);
-  if (rc) return rc;
-  if (!used) {
-    rc = from_cuda(launch_simt(r, s, st));
-    if (rc) return rc;
-  }
-  return from_cuda(launch_combine(r, s, p->dtype, st));
+  if (p->batch > 0 && (!k_new || !v_new || !k_lens || !k_cache || !v_cache)) return ATTN_ERR_INVALID_ARG;
+  if (p->batch > 0 && p->k_len < 1) return ATTN_ERR_INVALID_ARG;
+  const size_t es = elem_size(p->dtype);
+  if ((k_new && !aligned(k_new, es)) || (v_new && !aligned(v_new, es))) return ATTN_ERR_ALIGNMENT;
+  return attn::decode_impl(p, q, k_cache, v_cache, o, mask, nullptr, k_lens, lse, workspace, workspace_bytes,
+                           stream, k_new, v_new);
 }
 
 int attn_combine(int32_t n_splits, int32_t rows, int32_t head_dim, const float* part_o, const float* part_lse,

@@ -34,6 +34,8 @@ struct Problem {
   int kv_per_channel;            // 1: scales per (kv head, channel); 0: one scale each
   const float* k_scale;
   const float* v_scale;
+  const void* k_new;             // decode with append: new rows [B][G][D] in dtype (nullptr: none)
+  const void* v_new;
   Layout q, k, v, o, m;
   int64_t seg_bs, lse_bs, lse_hs;
   const void* Q;
@@ -129,6 +131,40 @@ __device__ __forceinline__ float fold_sink(float& m, float& l, float s) {
   l = fmaf(l, f, BASE2 ? ex2_approx(s - mx) : expf(s - mx));
   m = mx;
   return f;
+}
+
+// The cache update before a decode step with append: the new key and value
+// rows of (batch b, kv head g) go to cache row `row` (the entry's last valid
+// row).  Float caches take a copy; an int8 cache takes x / scale rounded to
+// the nearest integer (ties to even, IEEE float32 division) and saturated to
+// [-128, 127].  The block's threads share the D elements; the caller
+// synchronises before any of its threads or copies read the row.
+template <typename T>
+__device__ __forceinline__ void append_row(const Problem& p, int b, int g, int64_t row) {
+  const int64_t src = ((int64_t)b * p.G + g) * p.D;
+  const int64_t kd = p.k.off + (int64_t)b * p.k.bs + (int64_t)g * p.k.hs + row * p.k.rs;
+  const int64_t vd = p.v.off + (int64_t)b * p.v.bs + (int64_t)g * p.v.hs + row * p.v.rs;
+  const T* kn = static_cast<const T*>(p.k_new);
+  const T* vn = static_cast<const T*>(p.v_new);
+  for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
+    if (p.kv_int8) {
+      const int si = p.kv_per_channel ? g * p.D + d : 0;
+      const float ck = fminf(fmaxf(rintf(to_f32(kn[src + d]) / p.k_scale[si]), -128.f), 127.f);
+      const float cv = fminf(fmaxf(rintf(to_f32(vn[src + d]) / p.v_scale[si]), -128.f), 127.f);
+      const_cast<int8_t*>(static_cast<const int8_t*>(p.K))[kd + d] = (int8_t)ck;
+      const_cast<int8_t*>(static_cast<const int8_t*>(p.V))[vd + d] = (int8_t)cv;
+    } else {
+      const_cast<T*>(static_cast<const T*>(p.K))[kd + d] = kn[src + d];
+      const_cast<T*>(static_cast<const T*>(p.V))[vd + d] = vn[src + d];
+    }
+  }
+}
+
+// Row of the cache update for batch entry b (its clamped length minus one),
+// or -1 when the entry has no valid row.
+__device__ __forceinline__ int64_t append_target(const Problem& p, int b) {
+  const int64_t L = p.klens ? clamp64((int64_t)p.klens[b] + p.klens_plus, 0, p.Sk) : p.Sk;
+  return L - 1;
 }
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current

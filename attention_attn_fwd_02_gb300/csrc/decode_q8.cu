@@ -115,6 +115,18 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
   const int h0 = g * p.qpg + hc * kHeads;
   const int nh = min(kHeads, p.qpg - hc * kHeads);
 
+  // Decode with append: the CTAs of the range holding the new row quantise
+  // and write it first; the proxy fence orders those writes before this
+  // CTA's TMA reads.
+  if (p.k_new) {
+    const int64_t row = append_target(p, b);
+    if (row >= 0 && row / sp.split_len == split) {
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      append_row<T>(p, b, g, row);
+      __syncthreads();
+      if (tid == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+  }
   int64_t lo, hi;
   row_range(p, b, 0, lo, hi);
   const int64_t k_begin = (int64_t)split * sp.split_len;

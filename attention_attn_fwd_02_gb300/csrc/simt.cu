@@ -49,6 +49,13 @@ __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp
   const int split = (int)(blk / ((int64_t)p.B * p.G));
   const int b = bg / p.G, g = bg % p.G;
   const int D = p.D;
+  // Decode with append: every CTA of the range holding the new row writes it
+  // (the same values) before the first barrier below, so its own staging
+  // reads see it.
+  if (p.k_new) {
+    const int64_t row = append_target(p, b);
+    if (row >= 0 && row / sp.split_len == split) append_row<T>(p, b, g, row);
+  }
 
   const int64_t k0 = (int64_t)split * sp.split_len;
   const int64_t k1 = min((int64_t)p.Sk, k0 + (int64_t)sp.split_len);

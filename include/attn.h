@@ -215,6 +215,23 @@ ATTN_API int attn_decode_noalloc(const attn_problem* p, const void* q, const voi
                                  const void* v_cache, void* o, const float* mask, const int32_t* seg,
                                  const int32_t* k_lens, float* lse, attn_stream stream);
 
+/* Decode step with the cache update fused in ("com.microsoft.GroupQueryAttention":
+ * present_key / present_value sharing the past buffer; seqlens_k counts the new
+ * token; the int8 decode variant appends quantised rows).  Same as attn_decode,
+ * except that the caches are written: for every batch entry b with
+ * L_b = clamp(k_lens[b] (+1 under ATTN_KLENS_LAST_INDEX), 0, k_len) >= 1 and
+ * every kv head g, cache row L_b - 1 first takes the new rows
+ * k_new / v_new[(b * kv_heads + g) * head_dim ..] (device, contiguous
+ * [batch][kv_heads][head_dim], in dtype), and then the step attends over rows
+ * 0 .. L_b - 1 as attn_decode does.  An int8 cache (kv_dtype = ATTN_KV_INT8)
+ * stores x / scale rounded to the nearest integer (ties to even, float32
+ * division) and saturated to [-128, 127].  k_lens is required; seg is not
+ * taken.  The row is written by the kernels of the step itself (no separate
+ * copy kernel); the caches must not be read by other work while the step runs. */
+ATTN_API int attn_decode_append(const attn_problem* p, const void* q, const void* k_new, const void* v_new,
+                                void* k_cache, void* v_cache, void* o, const float* mask, const int32_t* k_lens,
+                                float* lse, void* workspace, size_t workspace_bytes, attn_stream stream);
+
 /* Size in bytes of the fixed scratch array attn_decode_noalloc uses. */
 ATTN_API size_t attn_decode_noalloc_max_scratch(void);
 

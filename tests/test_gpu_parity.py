@@ -14,7 +14,7 @@ import pytest
 import oracle
 from attention_attn_fwd_02_gb300 import attn, build
 from attention_attn_fwd_02_gb300 import workloads as wl
-from gpu_util import GpuCase, compare, oracle_full, torch_mod
+from gpu_util import GpuCase, compare, host_storage, oracle_full, torch_mod
 
 pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
 
@@ -433,3 +433,52 @@ def test_prefill_int8_cache_generic_path():
                      q_len=70, k_len=150, head_dim=64, causal=True, k_lens=np.array([150, 90], dtype=np.int32),
                      kv_dtype="i8", kv_scale="channel")
     run_and_compare(c)
+
+
+# ---- decode with the cache append fused in --------------------------------------------------------
+
+APPEND = [
+    # dtype, B, H, G, cap, D, kv_dtype, k_lens_kind
+    ("bf16", 4, 32, 8, 2500, 128, None, "count"),          # tensor-core pass
+    ("f16", 3, 8, 2, 700, 64, None, "last_index"),         # CUDA-core pass
+    ("bf16", 3, 16, 4, 2000, 128, "i8", "count"),          # int8 tensor-core pass (quantised append)
+    ("f16", 2, 6, 3, 500, 64, "i8", "last_index"),         # int8 CUDA-core pass
+]
+
+
+@pytest.mark.parametrize("i", range(len(APPEND)))
+def test_decode_with_cache_append(i):
+    """attn_decode_append writes each entry's new K/V row at its last valid
+    position (bit-exact against the oracle's append, int8 codes included) and
+    attends over the updated cache (parity with the oracle on that cache)."""
+    torch = torch_mod()
+    dtype, B, H, G, cap, D, kv, kind = APPEND[i]
+    r = np.random.default_rng(1400 + i)
+    counts = r.integers(1, cap + 1, size=B).astype(np.int32)
+    counts[0] = cap
+    stored = counts - 1 if kind == "last_index" else counts
+    c = wl.make_case(name=f"app{i}", seed=1500 + i, dtype=dtype, batch=B, heads=H, kv_heads=G, q_len=1, k_len=cap,
+                     head_dim=D, k_lens=stored, k_lens_kind=kind, decode=True, kv_dtype=kv, kv_scale="channel",
+                     nan_fill=False)
+    new = wl.to_storage(r.standard_normal((2, B, G, D)).astype(np.float32), dtype)
+    kn, vn = new[0], new[1]
+    g = GpuCase(c)
+    dk_new, dv_new = (torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).cuda() for x in (kn, vn))
+    need = attn.attn_decode_workspace_size(g.prob)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    rc = attn.attn_decode_append(g.prob, g.q.data_ptr(), dk_new.data_ptr(), dv_new.data_ptr(), g.k.data_ptr(),
+                                 g.v.data_ptr(), g.o.data_ptr(), None, g.k_lens.data_ptr(), g.lse.data_ptr(),
+                                 ws.data_ptr(), need, st)
+    assert rc == attn.ATTN_OK, attn.status_string(rc)
+    torch.cuda.synchronize()
+    k2, v2 = oracle.append_rows(c.problem, c.k, c.v, kn, vn, stored, k_scale=c.k_scale, v_scale=c.v_scale)
+    if kv is None:
+        gk, gv = host_storage(g.k, dtype), host_storage(g.v, dtype)
+    else:
+        gk, gv = g.k.cpu().numpy(), g.v.cpu().numpy()
+    assert np.array_equal(gk, k2.reshape(gk.shape)) and np.array_equal(gv, v2.reshape(gv.shape))
+    o, lse, _ = g.outputs()
+    ref_o, ref_l = oracle.attn(c.problem, c.q, k2, v2, k_lens=stored, k_scale=c.k_scale, v_scale=c.v_scale)
+    compare(o, lse, ref_o.reshape(o.shape), ref_l.reshape(lse.shape), dtype, "nan", f"append{i}")
+    assert attn.attn_device_status() == attn.ATTN_OK
