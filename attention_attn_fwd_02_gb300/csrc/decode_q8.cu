@@ -20,15 +20,17 @@
 // 0x80), whose value is 1024 + x + 128, minus 1152.
 //
 // Fragment layouts (mma.sync m16n8k16, f16 in, f32 accumulate; g = lane / 4,
-// t = lane % 4).  Q K^T sums over head-dim channels, so any permutation of
-// the 16 channels of a K-step that Q and K share gives the same S: thread t
-// takes channels 4t .. 4t+3 of each 16, i.e. one 32-bit word of a K row,
-// where the operand layout asks for channels 2t, 2t+1, 2t+8, 2t+9.  P V sums
-// over keys in their natural order (the S accumulators of two 8-key tiles are
-// the A operand), and the output column of n-tile j, lane column n is the
-// channel 32 (j / 4) + 4 n + j % 4, so a thread's four columns of a j-group are
-// one 32-bit word of a V row; four V rows (keys 2t, 2t+1, 2t+8, 2t+9) give it
-// the B operands of four n-tiles after byte permutes.
+// t = lane % 4).  The cache bytes are read with ldmatrix as if they were
+// 16-bit elements, two int8 values each.  Q K^T sums over head-dim channels,
+// so any permutation of the 16 channels of a K-step that Q and K share gives
+// the same S: thread t takes channels 4t .. 4t+3 of each 16 -- the 32-bit word
+// ldmatrix hands it from row g of an 8-key, 16-channel block -- where the
+// operand layout asks for channels 2t, 2t+1, 2t+8, 2t+9.  P V sums over keys
+// in their natural order (the S accumulators of two 8-key tiles are the A
+// operand).  ldmatrix.trans of an 8-key, 16-channel block hands thread (g, t)
+// keys 2t and 2t+1 of channels 2g and 2g+1; the even channel's pair is the B
+// operand of one n-tile and the odd channel's of another, so n-tile (c, q) of
+// channel block c has channel 16 c + 2 n + q in its column n.
 //
 // CTA: 4 warps; one (batch, kv head, key range) and up to 16 query heads of
 // that kv head (the MMA rows), so each cache byte is read once.  The range
@@ -87,11 +89,15 @@ __device__ __forceinline__ uint32_t bytes_to_h2(uint32_t biased, uint32_t sel) {
   h = __hsub2(h, __half2half2(__ushort_as_half((unsigned short)0x6480)));  // 1152
   return *reinterpret_cast<uint32_t*>(&h);
 }
-// Byte offset of (row, byte column c) in a 64-row, 128-byte-wide stage tile
-// written by TMA with 128-byte swizzle: the 16-byte unit u of a row sits at
-// u ^ (row % 8).
-__device__ __forceinline__ uint32_t sw8(int row, int c) {
-  return (uint32_t)(row * 128 + ((((c >> 4) ^ (row & 7))) << 4) + (c & 15));
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
 
 template <bool BF16>
@@ -210,20 +216,24 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
     if (!ok) break;
     consumed = ch + 1;
     const int64_t k0 = start + (int64_t)ch * kStageKeys + warp * 16;  // first key of this warp
-    const uint8_t* kt = smem + s * 2 * kTile;
-    const uint8_t* vt = smem + s * 2 * kTile + kTile;
-    const int rb = warp * 16;  // warp's first row in the stage tile
+    // ldmatrix row addresses: lane L supplies row (L % 8) of block L / 8 in a
+    // 128-byte-swizzled tile (16-byte unit u of row r at u ^ (r % 8)).
+    const uint32_t kt = su32(smem + s * 2 * kTile), vt = kt + kTile;
+    const int lrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);   // blocks alternate key halves
+    const uint32_t krow = kt + lrow * 128, vrow = vt + lrow * 128;
+    const int ublk = lane >> 4;                                       // blocks 2, 3: the next 16 channels
     // Rows past the range end need no clearing: their probabilities are 0 and
     // every int8 value is finite (rows past the capacity are zero-filled).
     // S = Q K^T for the warp's 16 keys (two n-tiles of 8 keys).
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int ds = 0; ds < 8; ++ds) {
+    for (int dp = 0; dp < 4; ++dp) {   // channel blocks 2 dp and 2 dp + 1
+      uint32_t kw[4];                  // (block 2dp, keys 0-7), (2dp, 8-15), (2dp+1, 0-7), (2dp+1, 8-15)
+      ldsm4(krow + (((2 * dp + ublk) ^ (lane & 7)) << 4), kw);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + sw8(rb + nt * 8 + gid, ds * 16 + tig * 4)) ^
-                           0x80808080u;
-        mma_f16(sc[nt], qa[ds], bytes_to_h2(w, 0x4140u), bytes_to_h2(w, 0x4342u));
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = kw[j] ^ 0x80808080u;
+        mma_f16(sc[j & 1], qa[2 * dp + (j >> 1)], bytes_to_h2(w, 0x4140u), bytes_to_h2(w, 0x4342u));
       }
     }
     // Scores in log2 units; keys past the end are hidden.
@@ -277,23 +287,21 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
       pa[2] = h2(pv[1][0], pv[1][1]);
       pa[3] = h2(pv[1][2], pv[1][3]);
     }
-    // O += P V: channel group q covers channels 32q .. 32q+31 (n-tiles 4q .. 4q+3);
-    // the thread reads channels 32q + 4 gid .. + 3 of keys 2 tig, 2 tig + 1,
-    // 2 tig + 8 and 2 tig + 9 of the warp's 16.
+    // O += P V over channel blocks of 16: ldmatrix.trans gives each thread
+    // [V(2t, 2g), V(2t, 2g+1), V(2t+1, 2g), V(2t+1, 2g+1)] of a block's keys
+    // 0-7 (and 8-15 in the next register); bytes 0 and 2 are the even
+    // channel's key pair, bytes 1 and 3 the odd channel's.
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int cb = q * 32 + gid * 4;
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vt + sw8(rb + 2 * tig, cb)) ^ 0x80808080u;
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vt + sw8(rb + 2 * tig + 1, cb)) ^ 0x80808080u;
-      const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vt + sw8(rb + 2 * tig + 8, cb)) ^ 0x80808080u;
-      const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vt + sw8(rb + 2 * tig + 9, cb)) ^ 0x80808080u;
-      // Interleave the bytes of key pairs: y01_lo = [w0.b0, w1.b0, w0.b1, w1.b1], y01_hi the upper bytes.
-      const uint32_t y01_lo = prmt(w0, w1, 0x5140u), y01_hi = prmt(w0, w1, 0x7362u);
-      const uint32_t y23_lo = prmt(w2, w3, 0x5140u), y23_hi = prmt(w2, w3, 0x7362u);
-      mma_f16(o[4 * q + 0], pa, bytes_to_h2(y01_lo, 0x4140u), bytes_to_h2(y23_lo, 0x4140u));
-      mma_f16(o[4 * q + 1], pa, bytes_to_h2(y01_lo, 0x4342u), bytes_to_h2(y23_lo, 0x4342u));
-      mma_f16(o[4 * q + 2], pa, bytes_to_h2(y01_hi, 0x4140u), bytes_to_h2(y23_hi, 0x4140u));
-      mma_f16(o[4 * q + 3], pa, bytes_to_h2(y01_hi, 0x4342u), bytes_to_h2(y23_hi, 0x4342u));
+    for (int cp = 0; cp < 4; ++cp) {   // channel blocks 2 cp and 2 cp + 1
+      uint32_t vw[4];                  // (block 2cp, keys 0-7), (2cp, 8-15), (2cp+1, 0-7), (2cp+1, 8-15)
+      ldsm4t(vrow + (((2 * cp + ublk) ^ (lane & 7)) << 4), vw);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t lo8 = vw[2 * j] ^ 0x80808080u, hi8 = vw[2 * j + 1] ^ 0x80808080u;
+        const int c = 2 * cp + j;
+        mma_f16(o[2 * c], pa, bytes_to_h2(lo8, 0x4240u), bytes_to_h2(hi8, 0x4240u));
+        mma_f16(o[2 * c + 1], pa, bytes_to_h2(lo8, 0x4341u), bytes_to_h2(hi8, 0x4341u));
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -326,10 +334,10 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
     if (hh < nh) {
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
-        // accumulator column n of n-tile nt is channel 32 (nt / 4) + 4 n + nt % 4
-        const int d0 = 32 * (nt >> 2) + 4 * (tig * 2) + (nt & 3);
+        // accumulator column n of n-tile nt = (block c, parity q) is channel 16 c + 2 n + q
+        const int d0 = 16 * (nt >> 1) + 2 * (tig * 2) + (nt & 1);
         red_acc[(warp * kHeads + hh) * kD + d0] = o[nt][2 * r];
-        red_acc[(warp * kHeads + hh) * kD + d0 + 4] = o[nt][2 * r + 1];
+        red_acc[(warp * kHeads + hh) * kD + d0 + 2] = o[nt][2 * r + 1];
       }
       if (tig == 0) {
         red_m[warp][hh] = m_ref[r];
