@@ -13,31 +13,37 @@
 // channel)).
 //
 // The scales leave the loop: Q . (k8 * s_k) = (Q * s_k) . k8, so Q is scaled
-// by the key scales once (per channel) and rounded to f16; and
+// by the key scales once (per channel), and by scale * log2(e) so that scores
+// come out in log2 units, then rounded to f16; and
 // sum p (v8 * s_v) = s_v * sum p v8, so the value scale multiplies the finished
-// partial O.  The integers themselves enter the tensor cores as f16, which
-// holds every int8 exactly: a byte x becomes the f16 with bits 0x6400 | (x ^
-// 0x80), whose value is 1024 + x + 128, minus 1152.
+// partial O.  The integers enter the tensor cores as exact f16 values with a
+// bias: a byte x becomes the f16 with bits 0x6400 | (x ^ 0x80), whose value is
+// x + 1152, one logic operation for two bytes.  The bias is taken out once, not
+// per element: S = sum Q'(x + 1152) - 1152 sum Q' (the accumulators start at
+// -1152 sum Q'), and O = sum p (x + 1152) - 1152 sum p, with sum p the sum of
+// the same rounded probabilities, accumulated by an MMA against ones.
 //
-// Fragment layouts (mma.sync m16n8k16, f16 in, f32 accumulate; g = lane / 4,
+// The query heads of a kv head are few (often 4 or 8), so the MMA puts the
+// keys on its 16 rows and the heads on its 8 columns: S^T = K Q'^T and
+// O^T = V^T P^T (mma.sync m16n8k16, f16 in, f32 accumulate; g = lane / 4,
 // t = lane % 4).  The cache bytes are read with ldmatrix as if they were
-// 16-bit elements, two int8 values each.  Q K^T sums over head-dim channels,
-// so any permutation of the 16 channels of a K-step that Q and K share gives
-// the same S: thread t takes channels 4t .. 4t+3 of each 16 -- the 32-bit word
-// ldmatrix hands it from row g of an 8-key, 16-channel block -- where the
-// operand layout asks for channels 2t, 2t+1, 2t+8, 2t+9.  P V sums over keys
-// in their natural order (the S accumulators of two 8-key tiles are the A
-// operand).  ldmatrix.trans of an 8-key, 16-channel block hands thread (g, t)
-// keys 2t and 2t+1 of channels 2g and 2g+1; the even channel's pair is the B
-// operand of one n-tile and the odd channel's of another, so n-tile (c, q) of
-// channel block c has channel 16 c + 2 n + q in its column n.
+// 16-bit elements, two int8 values each.  S^T sums over head-dim channels, so
+// any permutation of the 16 channels of a K-step that K and Q share gives the
+// same S: ldmatrix hands thread t the word of channels 4t .. 4t+3 of key rows
+// g and g + 8, whose bytes 0 and 2 are the operand's k = 2t, 2t + 1 and bytes 1
+// and 3 its k = 2t + 8, 2t + 9; Q' follows the same order.  The S^T
+// accumulator (keys g, g+8 x heads 2t, 2t+1), rounded to f16, is moved into
+// the B operand of P^T (keys 2t, 2t+1 (+8) x head g) by movmatrix.trans.
+// ldmatrix.trans of an 8-key, 16-channel block hands thread (g, t) keys 2t
+// and 2t+1 of channels 2g and 2g+1: the even channel's pair is row g of the
+// V^T operand, the odd channel's row g + 8.
 //
-// CTA: 4 warps; one (batch, kv head, key range) and up to 16 query heads of
-// that kv head (the MMA rows), so each cache byte is read once.  The range
-// streams through shared memory in 64-key stages, three deep (48 KB, so four
-// CTAs share an SM), copied by TMA with 128-byte swizzle (conflict-free
-// 32-bit reads); warp w takes keys 16w .. 16w+15 of a stage.  Waits are
-// bounded (status word on timeout).
+// CTA: 4 warps; one (batch, kv head, key range) and up to 8 (or 16, two MMA
+// column tiles) query heads of that kv head, so each cache byte is read once.
+// The range streams through shared memory in 64-key stages, three deep
+// (48 KB), copied by TMA with 128-byte swizzle (conflict-free ldmatrix);
+// warp w takes keys 16w .. 16w+15 of a stage.  Waits are bounded (status word
+// on timeout).
 #include <stdlib.h>
 
 #include <type_traits>
@@ -63,7 +69,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kStageKeys = 64;
 constexpr int kStages = 3;
 constexpr int kTile = kStageKeys * kD;   // bytes of the K (or V) tile of a stage
-constexpr int kHeads = 16;               // query heads per CTA (MMA rows)
+constexpr float kBias = 1152.f;          // the f16 value of a biased int8 0
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kSlack = 8.0f;
@@ -75,19 +81,16 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+// Two int8 values of a word (bytes 0 and 2, or 1 and 3) as an f16 pair with
+// exponent byte 0x64 and the byte XOR 0x80 as its low mantissa bits: the
+// value 1024 + (x + 128) = x + kBias, exact, in one logic operation.
+__device__ __forceinline__ uint32_t bias_lo(uint32_t w) { return (w & 0x00FF00FFu) ^ 0x64806480u; }
+__device__ __forceinline__ uint32_t bias_hi(uint32_t w) { return ((w >> 8) & 0x00FF00FFu) ^ 0x64806480u; }
+// Transpose of an 8x8 matrix of 16-bit values held one row pair per thread.
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
   return r;
-}
-// Two biased bytes (already XOR 0x80) at the byte slots picked by sel, placed
-// as the low halves of an f16 pair with exponent byte 0x64, minus 1152: the
-// original signed integers as an exact f16 pair.
-__device__ __forceinline__ uint32_t bytes_to_h2(uint32_t biased, uint32_t sel) {
-  const uint32_t w = prmt(biased, 0x64646464u, sel);
-  __half2 h = *reinterpret_cast<const __half2*>(&w);
-  h = __hsub2(h, __half2half2(__ushort_as_half((unsigned short)0x6480)));  // 1152
-  return *reinterpret_cast<uint32_t*>(&h);
 }
 __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -100,15 +103,16 @@ __device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
-template <bool BF16>
+template <bool BF16, int NT>
 __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v,
                                                              const Problem p, const Split sp, const int n_hc) {
+  constexpr int kHc = 8 * NT;   // query heads per CTA (MMA columns)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ int abort_flag;
-  __shared__ float red_m[kWarps][kHeads], red_l[kWarps][kHeads];
+  __shared__ float red_m[kWarps][kHc], red_l[kWarps][kHc];
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, gid = lane >> 2, tig = lane & 3;
   int64_t blk = blockIdx.x;
@@ -118,8 +122,8 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
   blk /= n_hc;
   const int g = (int)(blk % p.G);
   const int b = (int)(blk / p.G);
-  const int h0 = g * p.qpg + hc * kHeads;
-  const int nh = min(kHeads, p.qpg - hc * kHeads);
+  const int h0 = g * p.qpg + hc * kHc;
+  const int nh = min(kHc, p.qpg - hc * kHc);
 
   // Decode with append: the CTAs of the range holding the new row quantise
   // and write it first; the proxy fence orders those writes before this
@@ -171,41 +175,74 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
     for (; issued < min(kStages, n_chunks); ++issued) issue(issued);
 
   const bool per_channel = p.kv_per_channel != 0;
-  // Q scaled by the key scales, as f16 A operands: rows = heads (gid, gid + 8),
-  // K-step ds covers channels 16 ds .. 16 ds + 15, thread tig takes channels
-  // 16 ds + 4 tig .. + 3 (see the layout note above).
-  uint32_t qa[8][4];
+  // Q' = Q * k_scale * scale * log2(e) as f16 B operands (n = head, k =
+  // channel): head 8j + gid, channel block c; b0 holds channels 16c + 4tig and
+  // + 2, b1 channels + 1 and + 3 (the order the K bytes arrive in).  qs sums
+  // the thread's rounded Q' values, for the bias correction below.
+  uint32_t qb[NT][8][2];
+  float kinit[NT][2];
   {
     using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     const T* Q = static_cast<const T*>(p.Q);
-    auto q2 = [&](int hh, int d) -> uint32_t {
-      if (hh >= nh) return 0u;
-      const int64_t base = p.q.off + (int64_t)b * p.q.bs + (int64_t)(h0 + hh) * p.q.hs + d;
-      const float s0 = p.k_scale[per_channel ? g * kD + d : 0];
-      const float s1 = p.k_scale[per_channel ? g * kD + d + 1 : 0];
-      __half2 v = __floats2half2_rn(to_f32(Q[base]) * s0, to_f32(Q[base + 1]) * s1);
-      return *reinterpret_cast<uint32_t*>(&v);
-    };
+    const float cs = p.scale * kLog2e;
 #pragma unroll
-    for (int ds = 0; ds < 8; ++ds) {
-      const int d = ds * 16 + tig * 4;
-      qa[ds][0] = q2(gid, d);
-      qa[ds][1] = q2(gid + 8, d);
-      qa[ds][2] = q2(gid, d + 2);
-      qa[ds][3] = q2(gid + 8, d + 2);
+    for (int j = 0; j < NT; ++j) {
+      const int hh = 8 * j + gid;
+      float qs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int d = 16 * c + 4 * tig;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (hh < nh) {
+          const int64_t base = p.q.off + (int64_t)b * p.q.bs + (int64_t)(h0 + hh) * p.q.hs + d;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            v[e] = __half2float(__float2half_rn(to_f32(Q[base + e]) * p.k_scale[per_channel ? g * kD + d + e : 0] * cs));
+        }
+        qs += (v[0] + v[1]) + (v[2] + v[3]);
+        __half2 h02 = __floats2half2_rn(v[0], v[2]), h13 = __floats2half2_rn(v[1], v[3]);
+        qb[j][c][0] = *reinterpret_cast<uint32_t*>(&h02);
+        qb[j][c][1] = *reinterpret_cast<uint32_t*>(&h13);
+      }
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      // The accumulator columns of this thread are heads 8j + 2tig and + 1.
+      const float q0 = __shfl_sync(0xffffffffu, qs, 8 * tig);
+      const float q1 = __shfl_sync(0xffffffffu, qs, 8 * tig + 4);
+      kinit[j][0] = -kBias * q0;
+      kinit[j][1] = -kBias * q1;
     }
   }
-  const float c = p.scale * kLog2e;
   const bool capped = p.softcap > 0.f;
-  const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
+  const float kinv = capped ? 1.f / (p.softcap * kLog2e) : 0.f, cap2 = p.softcap * kLog2e;
   const float* mrow = p.M ? p.M + p.m.off + (int64_t)b * p.m.bs : nullptr;
+  const bool plain = !capped && !mrow;
 
-  float o[16][4];
+  // O^T accumulators: o[c][j] rows = channels 16c + 2gid (rows gid) and
+  // 16c + 2gid + 1 (rows gid + 8), columns = heads 8j + 2tig, + 1.  ls[j]
+  // accumulates the rounded probabilities themselves (same columns).
+  float o[8][NT][4], ls[NT][4];
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
+  for (int c = 0; c < 8; ++c)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
-  float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[c][j][e] = 0.f;
+  float m_ref[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    m_ref[j][0] = m_ref[j][1] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ls[j][e] = 0.f;
+  }
+  const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+
+  // ldmatrix row addresses: lane L supplies row (L % 8) of block L / 8 in a
+  // 128-byte-swizzled tile (16-byte unit u of row r at u ^ (r % 8)); blocks
+  // alternate the warp's two 8-key halves, blocks 2 and 3 take the next 16
+  // channels.
+  const int lrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int ublk = lane >> 4;
 
   bool ok = true;
   int consumed = 0;
@@ -216,93 +253,92 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
     if (!ok) break;
     consumed = ch + 1;
     const int64_t k0 = start + (int64_t)ch * kStageKeys + warp * 16;  // first key of this warp
-    // ldmatrix row addresses: lane L supplies row (L % 8) of block L / 8 in a
-    // 128-byte-swizzled tile (16-byte unit u of row r at u ^ (r % 8)).
-    const uint32_t kt = su32(smem + s * 2 * kTile), vt = kt + kTile;
-    const int lrow = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);   // blocks alternate key halves
-    const uint32_t krow = kt + lrow * 128, vrow = vt + lrow * 128;
-    const int ublk = lane >> 4;                                       // blocks 2, 3: the next 16 channels
+    const uint32_t krow = su32(smem + s * 2 * kTile) + lrow * 128, vrow = krow + kTile;
     // Rows past the range end need no clearing: their probabilities are 0 and
     // every int8 value is finite (rows past the capacity are zero-filled).
-    // S = Q K^T for the warp's 16 keys (two n-tiles of 8 keys).
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S^T = K Q'^T for the warp's 16 keys (MMA rows: keys gid, gid + 8),
+    // started at the bias correction so that it holds the scores in log2 units.
+    float st[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      st[j][0] = st[j][2] = kinit[j][0];
+      st[j][1] = st[j][3] = kinit[j][1];
+    }
 #pragma unroll
     for (int dp = 0; dp < 4; ++dp) {   // channel blocks 2 dp and 2 dp + 1
       uint32_t kw[4];                  // (block 2dp, keys 0-7), (2dp, 8-15), (2dp+1, 0-7), (2dp+1, 8-15)
       ldsm4(krow + (((2 * dp + ublk) ^ (lane & 7)) << 4), kw);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t w = kw[j] ^ 0x80808080u;
-        mma_f16(sc[j & 1], qa[2 * dp + (j >> 1)], bytes_to_h2(w, 0x4140u), bytes_to_h2(w, 0x4342u));
+      for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t a[4] = {bias_lo(kw[2 * jj]), bias_lo(kw[2 * jj + 1]), bias_hi(kw[2 * jj]),
+                               bias_hi(kw[2 * jj + 1])};
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_f16(st[j], a, qb[j][2 * dp + jj][0], qb[j][2 * dp + jj][1]);
       }
     }
-    // Scores in log2 units; keys past the end are hidden.
+    // Transforms and hiding of keys past the end (warp-uniform skip for whole
+    // in-range tiles without softcap or mask).
+    if (!plain || k0 + 16 > end) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int j = 0; j < NT; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int64_t key = k0 + nt * 8 + tig * 2 + (e & 1);
-        const int hh = gid + (e >> 1) * 8;
-        float x = capped ? cap2 * tanh_exp2(sc[nt][e] * kinv) : sc[nt][e] * c;
-        if (mrow && key < end && hh < nh) x = fmaf(mrow[(int64_t)(h0 + hh) * p.m.hs + key], kLog2e, x);
-        sc[nt][e] = key < end ? x : -INFINITY;
-      }
-    // Per head row: maximum over the 16 keys (a quad of lanes shares a row).
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float mx = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      if (mx > m_ref[r] + kSlack) {
-        const float corr = ex2_approx(m_ref[r] - mx);
-        l[r] *= corr;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          o[nt][2 * r] *= corr;
-          o[nt][2 * r + 1] *= corr;
+        for (int e = 0; e < 4; ++e) {
+          const int64_t key = k0 + gid + 8 * (e >> 1);
+          const int hh = 8 * j + 2 * tig + (e & 1);
+          float x = capped ? cap2 * tanh_exp2(st[j][e] * kinv) : st[j][e];
+          if (mrow && key < end && hh < nh) x = fmaf(mrow[(int64_t)(h0 + hh) * p.m.hs + key], kLog2e, x);
+          st[j][e] = key < end ? x : -INFINITY;
         }
-        m_ref[r] = mx;
-      }
     }
-    uint32_t pa[4];
-    {
-      const float mu0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
-      const float mu1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
-      float pv[2][4];
+    uint32_t pb[NT][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        pv[nt][0] = ex2_approx(sc[nt][0] - mu0);
-        pv[nt][1] = ex2_approx(sc[nt][1] - mu0);
-        pv[nt][2] = ex2_approx(sc[nt][2] - mu1);
-        pv[nt][3] = ex2_approx(sc[nt][3] - mu1);
+    for (int j = 0; j < NT; ++j) {
+      // Per head column: maximum over the 16 keys (the eight lanes of a tig).
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float mx = fmaxf(st[j][q], st[j][q + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (mx > m_ref[j][q] + kSlack) {
+          const float corr = ex2_approx(m_ref[j][q] - mx);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            o[c][j][q] *= corr;
+            o[c][j][q + 2] *= corr;
+          }
+          ls[j][q] *= corr;
+          ls[j][q + 2] *= corr;
+          m_ref[j][q] = mx;
+        }
       }
-      l[0] += (pv[0][0] + pv[0][1]) + (pv[1][0] + pv[1][1]);
-      l[1] += (pv[0][2] + pv[0][3]) + (pv[1][2] + pv[1][3]);
-      auto h2 = [](float lo_, float hi_) {
-        __half2 v = __floats2half2_rn(lo_, hi_);
-        return *reinterpret_cast<uint32_t*>(&v);
-      };
-      pa[0] = h2(pv[0][0], pv[0][1]);
-      pa[1] = h2(pv[0][2], pv[0][3]);
-      pa[2] = h2(pv[1][0], pv[1][1]);
-      pa[3] = h2(pv[1][2], pv[1][3]);
+      const float mu0 = m_ref[j][0] == -INFINITY ? 0.f : m_ref[j][0];
+      const float mu1 = m_ref[j][1] == -INFINITY ? 0.f : m_ref[j][1];
+      __half2 p01 = __floats2half2_rn(ex2_approx(st[j][0] - mu0), ex2_approx(st[j][1] - mu1));
+      __half2 p23 = __floats2half2_rn(ex2_approx(st[j][2] - mu0), ex2_approx(st[j][3] - mu1));
+      // P as an 8-key x 8-head matrix per key half; transposed, it is the B
+      // operand (k = keys 2tig, 2tig + 1 (+ 8), n = head gid).
+      pb[j][0] = movtrans(*reinterpret_cast<uint32_t*>(&p01));
+      pb[j][1] = movtrans(*reinterpret_cast<uint32_t*>(&p23));
     }
-    // O += P V over channel blocks of 16: ldmatrix.trans gives each thread
+    // O^T += V^T P^T over channel blocks of 16: ldmatrix.trans gives each thread
     // [V(2t, 2g), V(2t, 2g+1), V(2t+1, 2g), V(2t+1, 2g+1)] of a block's keys
-    // 0-7 (and 8-15 in the next register); bytes 0 and 2 are the even
-    // channel's key pair, bytes 1 and 3 the odd channel's.
+    // 0-7 (and 8-15 in the next register); bytes 0 and 2 are channel 2g's key
+    // pair (MMA row gid), bytes 1 and 3 channel 2g+1's (row gid + 8).
 #pragma unroll
     for (int cp = 0; cp < 4; ++cp) {   // channel blocks 2 cp and 2 cp + 1
       uint32_t vw[4];                  // (block 2cp, keys 0-7), (2cp, 8-15), (2cp+1, 0-7), (2cp+1, 8-15)
       ldsm4t(vrow + (((2 * cp + ublk) ^ (lane & 7)) << 4), vw);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const uint32_t lo8 = vw[2 * j] ^ 0x80808080u, hi8 = vw[2 * j + 1] ^ 0x80808080u;
-        const int c = 2 * cp + j;
-        mma_f16(o[2 * c], pa, bytes_to_h2(lo8, 0x4240u), bytes_to_h2(hi8, 0x4240u));
-        mma_f16(o[2 * c + 1], pa, bytes_to_h2(lo8, 0x4341u), bytes_to_h2(hi8, 0x4341u));
+      for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t a[4] = {bias_lo(vw[2 * jj]), bias_hi(vw[2 * jj]), bias_lo(vw[2 * jj + 1]),
+                               bias_hi(vw[2 * jj + 1])};
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_f16(o[2 * cp + jj][j], a, pb[j][0], pb[j][1]);
       }
     }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) mma_f16(ls[j], ones, pb[j][0], pb[j][1]);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     if (tid == 0 && issued < n_chunks) {
@@ -321,30 +357,28 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
   ok = __syncthreads_and(ok && !*(volatile int*)&abort_flag);
   if (!ok) return;
 
-  // Row sums over the quad, then merge the four warps in order.
+  // Per warp: the biased values sum to O + 1152 * l, so subtract the bias
+  // times the probability sum; then merge the four warps in order.
+  float* red_acc = reinterpret_cast<float*>(smem);  // [kWarps][kHc][kD], by channel
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-  }
-  float* red_acc = reinterpret_cast<float*>(smem);  // [kWarps][kHeads][kD], by channel
+  for (int j = 0; j < NT; ++j)
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int hh = gid + 8 * r;
-    if (hh < nh) {
+    for (int q = 0; q < 2; ++q) {
+      const int hh = 8 * j + 2 * tig + q;
+      if (hh < nh) {
+        const float corr = kBias * ls[j][q];
+        float* dst = red_acc + (warp * kHc + hh) * kD + 2 * gid;
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        // accumulator column n of n-tile nt = (block c, parity q) is channel 16 c + 2 n + q
-        const int d0 = 16 * (nt >> 1) + 2 * (tig * 2) + (nt & 1);
-        red_acc[(warp * kHeads + hh) * kD + d0] = o[nt][2 * r];
-        red_acc[(warp * kHeads + hh) * kD + d0 + 2] = o[nt][2 * r + 1];
-      }
-      if (tig == 0) {
-        red_m[warp][hh] = m_ref[r];
-        red_l[warp][hh] = l[r];
+        for (int c = 0; c < 8; ++c) {
+          dst[16 * c] = o[c][j][q] - corr;
+          dst[16 * c + 1] = o[c][j][q + 2] - corr;
+        }
+        if (gid == 0) {
+          red_m[warp][hh] = m_ref[j][q];
+          red_l[warp][hh] = ls[j][q];
+        }
       }
     }
-  }
   __syncthreads();
   for (int i = tid; i < nh * kD; i += kThreads) {
     const int hh = i / kD, d = i % kD;
@@ -359,7 +393,7 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
       for (int w = 0; w < kWarps; ++w) {
         const float f = ex2_approx(red_m[w][hh] - M);
         L = fmaf(f, red_l[w][hh], L);
-        a = fmaf(f, red_acc[(w * kHeads + hh) * kD + d], a);
+        a = fmaf(f, red_acc[(w * kHc + hh) * kD + d], a);
       }
       ov = a / L * p.v_scale[per_channel ? g * kD + d : 0];
       lse = (M + __log2f(L)) * kLn2;
@@ -369,20 +403,25 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
   }
 }
 
-template <bool BF16>
+template <bool BF16, int NT>
 int launch(const Problem& p, const Split& s, cudaStream_t st) {
   CUtensorMap mk, mv;
   if (!tma_map_bhsd_u8(&mk, p.K, kD, p.Sk, p.G, p.B, p.k, kStageKeys) ||
       !tma_map_bhsd_u8(&mv, p.V, kD, p.Sk, p.G, p.B, p.v, kStageKeys))
     return -1;
-  const int n_hc = (p.qpg + kHeads - 1) / kHeads;
+  const int n_hc = (p.qpg + 8 * NT - 1) / (8 * NT);
   const int64_t blocks = (int64_t)s.n_splits * n_hc * p.G * p.B;
   if (blocks <= 0 || blocks > 0x7fffffff) return -1;
   const int smem = kStages * 2 * kTile + 1024;
-  auto kern = decode_q8_kernel<BF16>;
+  auto kern = decode_q8_kernel<BF16, NT>;
   if (ensure_smem((const void*)kern, smem) != cudaSuccess) return ATTN_ERR_CUDA;
   kern<<<(unsigned)blocks, kThreads, smem, st>>>(mk, mv, p, s, n_hc);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <bool BF16>
+int launch(const Problem& p, const Split& s, cudaStream_t st) {
+  return p.qpg <= 8 ? launch<BF16, 1>(p, s, st) : launch<BF16, 2>(p, s, st);
 }
 
 }  // namespace dq8

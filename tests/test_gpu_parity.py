@@ -406,6 +406,8 @@ INT8 = [
     ("bf16", 2, 40, 2, 2100, 128, "channel", False, dict(softcap=2.0, head_sink="heads",
                                                           window_left=700)),               # with transforms
     ("bf16", 2, 8, 2, 900, 64, "channel", True, {}),                                       # generic pass
+    ("bf16", 3, 64, 8, 1200, 128, "channel", True, {}),                                    # 8 heads: one MMA column tile
+    ("f16", 2, 64, 4, 2500, 128, "tensor", False, {}),                                     # 16 heads: two column tiles
 ]
 
 
