@@ -202,52 +202,72 @@ __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp
 // One warp per row: merge the row's range partials in range order.
 // With sink_on the head's sink logit enters as one more range with an
 // empty numerator (the sink term of the denominator, added once per row).
+// The lanes read the ranges' LSEs in parallel (lane r: ranges r, r + 32, ...)
+// and broadcast the weights; the partial rows of four ranges are loaded
+// before they are summed, so the loads overlap instead of queueing behind one
+// another.  Ranges with weight 0 (empty, or underflowed) are left out of the
+// sum by a select, so an unwritten partial never reaches it.
 template <typename T>
 __global__ void __launch_bounds__(128) combine_kernel(int n_splits, int64_t rows, int D, const float* part_o,
                                                       const float* part_lse, T* O, Layout ol, int H, int Sq,
                                                       float* lse, int64_t lse_bs, int64_t lse_hs,
                                                       int64_t lse_rs, int masked_zero, int sink_on,
                                                       const float* sink) {
+  constexpr unsigned kAll = 0xffffffffu;
   const int64_t row = (int64_t)blockIdx.x * 4 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= rows) return;
   const float* pl = part_lse + row * n_splits;
-  float M = -INFINITY;
-  bool bad = false;
-  for (int r = 0; r < n_splits; ++r) {
+  const int i = (int)(row % Sq);
+  const int h = (int)((row / Sq) % H);
+  const float sg = sink_on ? (sink ? sink[h] : 0.f) : -INFINITY;
+  bool bad = isnan(sg) || sg == INFINITY;
+  float M = bad ? -INFINITY : sg;
+  for (int r = lane; r < n_splits; r += 32) {
     const float x = pl[r];
     if (isnan(x) || x == INFINITY) bad = true;
     else M = fmaxf(M, x);
   }
-  const int i = (int)(row % Sq);
-  const int h = (int)((row / Sq) % H);
-  const float sg = sink_on ? (sink ? sink[h] : 0.f) : -INFINITY;
-  if (isnan(sg) || sg == INFINITY) bad = true;
-  else M = fmaxf(M, sg);
+  bad = __any_sync(kAll, bad);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, o));
   const int64_t b = row / ((int64_t)Sq * H);
   const int64_t ob = ol.off + b * ol.bs + (int64_t)h * ol.hs + (int64_t)i * ol.rs;
+  const bool normal = !bad && M != -INFINITY;
   float acc[8];
 #pragma unroll
   for (int s = 0; s < 8; ++s) acc[s] = 0.f;
   float ws = 0.f;
-  if (!bad && M != -INFINITY) {
-    if (sg > -INFINITY) ws = expf(sg - M);
-    for (int r = 0; r < n_splits; ++r) {
-      const float x = pl[r];
-      if (x == -INFINITY) continue;
-      const float w = expf(x - M);
-      ws += w;
-      const float* src = part_o + (row * n_splits + r) * D;
+  if (normal) {
+    for (int base = 0; base < n_splits; base += 32) {
+      const int r = base + lane;
+      const float x = r < n_splits ? pl[r] : -INFINITY;
+      const float wr = x == -INFINITY ? 0.f : expf(x - M);
+      ws += wr;
+      const int nr = min(32, n_splits - base);
+      for (int k = 0; k < nr; k += 4) {
+        float w[4], v[4][8];
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const int d = lane + 32 * s;
-        if (d < D) acc[s] = fmaf(w, src[d], acc[s]);
+        for (int u = 0; u < 4; ++u) {
+          w[u] = __shfl_sync(kAll, wr, k + u);   // lanes past the last range hold 0
+          const float* src = part_o + (row * n_splits + min(base + k + u, n_splits - 1)) * D;
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const int d = lane + 32 * s;
+            v[u][s] = d < D ? src[d] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int s = 0; s < 8; ++s) acc[s] = w[u] != 0.f ? fmaf(w[u], v[u][s], acc[s]) : acc[s];
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(kAll, ws, o);
+    if (sg > -INFINITY) ws += expf(sg - M);
   }
-  float val_fill = NAN;
-  if (!bad && M == -INFINITY) val_fill = masked_zero ? 0.f : NAN;
-  const bool normal = !bad && M != -INFINITY;
+  const float val_fill = (!bad && M == -INFINITY) ? (masked_zero ? 0.f : NAN) : NAN;
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const int d = lane + 32 * s;

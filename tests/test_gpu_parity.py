@@ -173,16 +173,20 @@ def test_hidden_keys_filled_with_nan_are_not_read():
     assert st["nan_rows"] == 0
 
 
-def test_combine_matches_oracle():
+@pytest.mark.parametrize("n,D", [(5, 72), (37, 256), (70, 40), (1, 128)])
+def test_combine_matches_oracle(n, D):
+    """Range counts below, across and beyond one warp's width; the partial rows
+    of empty ranges (lse -inf) hold NaN, which must not reach the sum."""
     torch = torch_mod()
-    r = np.random.default_rng(51)
-    rows, n, D = 37, 5, 72
+    r = np.random.default_rng(51 + n)
+    rows = 37
     po = r.standard_normal((rows, n, D)).astype(np.float32)
     pl = (r.standard_normal((rows, n)) * 3).astype(np.float32)
     pl[r.random((rows, n)) < 0.3] = -np.inf
     pl[3] = -np.inf
-    pl[4, 2] = np.nan
-    pl[5, 1] = np.inf
+    pl[4, n // 2] = np.nan
+    pl[5, n - 1] = np.inf
+    po[np.isneginf(pl)] = np.nan
     for mr in ("nan", "zero"):
         ref_o, ref_l = oracle.combine(po, pl, masked_rows=mr)
         for dt, tol in ((torch.float32, 1e-6), (torch.bfloat16, 1.5e-2)):
