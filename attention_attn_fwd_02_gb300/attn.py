@@ -27,7 +27,7 @@ ATTN_KV_SCALE_TENSOR, ATTN_KV_SCALE_CHANNEL = 0, 1
 DTYPE_CODE = {"f32": ATTN_F32, "f16": ATTN_F16, "bf16": ATTN_BF16}
 EXPORTS = ("attn_fwd_workspace_size", "attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_combine",
            "attn_device_status", "attn_status_string", "attn_version", "attn_decode_noalloc",
-           "attn_decode_noalloc_max_scratch", "attn_decode_append")
+           "attn_decode_noalloc_max_scratch", "attn_decode_append", "attn_probe_ex2")
 
 
 class attn_layout(ctypes.Structure):
@@ -85,6 +85,7 @@ def lib():
         L.attn_decode_noalloc_max_scratch.argtypes, L.attn_decode_noalloc_max_scratch.restype = [], sz
         L.attn_decode_append.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.attn_decode_append.restype = ctypes.c_int
+        L.attn_probe_ex2.argtypes, L.attn_probe_ex2.restype = [i32, i32, vp, vp], ctypes.c_int
         _lib = L
     return _lib
 
@@ -119,6 +120,11 @@ def attn_decode_append(p, q, k_new, v_new, k_cache, v_cache, o, mask, k_lens, ls
                        stream) -> int:
     return lib().attn_decode_append(ctypes.byref(p), q, k_new, v_new, k_cache, v_cache, o, mask, k_lens, lse,
                                     workspace, workspace_bytes, stream)
+
+
+def attn_probe_ex2(blocks, iters, sink, stream) -> int:
+    """Launch the exponential-throughput micro-kernel (a measurement utility; see include/attn.h)."""
+    return lib().attn_probe_ex2(blocks, iters, sink, stream)
 
 
 def attn_decode_noalloc_max_scratch() -> int:

@@ -319,6 +319,11 @@ const char* attn_status_string(int status) {
   }
 }
 
-int attn_version(void) { return 220; }
+int attn_probe_ex2(int32_t blocks, int32_t iters, float* sink, attn_stream stream) {
+  if (blocks < 1 || iters < 1 || !sink || !aligned(sink, 4)) return ATTN_ERR_INVALID_ARG;
+  return from_cuda(launch_ex2_probe(blocks, iters, sink, static_cast<cudaStream_t>(stream)));
+}
+
+int attn_version(void) { return 230; }
 
 }  // extern "C"

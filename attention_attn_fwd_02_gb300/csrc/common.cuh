@@ -196,6 +196,7 @@ inline cudaError_t ensure_smem(const void* kern, int bytes) {
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_simt(const Problem& p, const Split& s, cudaStream_t st);
 cudaError_t launch_combine(const Problem& p, const Split& s, int32_t out_dtype, cudaStream_t st);
+cudaError_t launch_ex2_probe(int blocks, int iters, float* sink, cudaStream_t st);
 cudaError_t launch_combine_flat(int n_splits, int rows, int D, const float* part_o, const float* part_lse,
                                 int32_t out_dtype, void* o, int64_t o_row_stride, float* lse,
                                 int masked_zero, cudaStream_t st);

@@ -73,6 +73,29 @@ def max_over_ranks(values, world: int, device=None):
     return [float(x) for x in t.cpu()]
 
 
+def ex2_rate(torch, attn, dev) -> float:
+    """Exponentials per second of the whole GPU, from the library's ex2 probe
+    (8 CTAs of 256 threads per SM, 8 chains a thread), best of three timed
+    launches after one warm-up."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = 8 * sms, 2048
+    sink = torch.empty(blocks, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream(dev)
+    best = None
+    for rep in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        rc = attn.attn_probe_ex2(blocks, iters, sink.data_ptr(), st.cuda_stream)
+        e1.record(st)
+        if rc:
+            raise attn.AttnError(rc, "attn_probe_ex2")
+        e1.synchronize()
+        if rep:
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+    return blocks * 256.0 * iters * 8 / (best / 1e3)
+
+
 def job_throughput(units_per_rank: float, world: int, steps: int, slowest_seconds: float) -> float:
     """Whole-job throughput: the units every rank processed over the slowest rank's time."""
     return world * steps * units_per_rank / slowest_seconds
@@ -414,6 +437,16 @@ def run_ours(args):
                 "traffic": ncu_traffic("decode_split", source_digest("decode.cu", "simt.cu")),
                 "peak_kind": f"{pk_kind} HBM copy", "frac_of_8tbs_spec": kv_bytes / (dec_s / steps) / 8e12,
                 "algorithmic_bytes_per_launch": kv_bytes}
+    # Exponential co-roofline: one exponential per visible pair (taken after the timed region).
+    exp_roof = None
+    if args.only != "decode":
+        rate = ex2_rate(torch, attn, dev)
+        sm_mhz = (clk.summary() or {}).get("sm_mhz")
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        pps = pairs / pre_launch_s
+        exp_roof = {"ex2_per_s": rate, "pairs_per_s": pps, "frac": pps / rate,
+                    "ex2_per_clock_per_sm": rate / (sms * sm_mhz * 1e6) if sm_mhz else None,
+                    "basis": "one exponential per visible pair; ex2 probe kernel, 8 chains per thread"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only is None:
         import oracle
@@ -430,6 +463,7 @@ def run_ours(args):
                    "visible_pairs": pairs, "decode_kv_bytes": kv_bytes, "l2": "flushed (256 MiB write) between steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": None if args.only == "decode" else roof,
+        "exp_roofline": exp_roof,
         "decode": (None if args.only == "prefill" else
                {"value": dec_gbs, "unit": "GB/s", "ms_per_step": 1e3 * dec_s / steps, "roofline": dec_roof}),
         "prefill_ms_per_step": 1e3 * pre_s / steps,

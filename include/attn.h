@@ -256,6 +256,19 @@ ATTN_API int attn_device_status(attn_stream stream);
 /* Static description of a status code. */
 ATTN_API const char* attn_status_string(int status);
 
+/* Measurement utility, not part of the attention path.  The softmax takes one
+ * base-2 exponential per visible query-key pair ("Attention", opening
+ * paragraph), so the hardware exponential's throughput bounds the prefill
+ * beside the tensor cores.  This launches `blocks` CTAs of 256 threads on
+ * `stream`; every thread evaluates `iters` x 8 approximate exponentials
+ * (ex2.approx, eight independent chains) and each CTA writes one float to
+ * sink[blockIdx] (device, float32 [blocks], 4-byte aligned, caller-owned) so
+ * the work is kept.  The caller times the launch with events: the rate is
+ * blocks * 256 * iters * 8 / time.  Returns ATTN_ERR_INVALID_ARG for
+ * blocks < 1, iters < 1 or a null or misaligned sink; ATTN_ERR_CUDA if the
+ * launch fails. */
+ATTN_API int attn_probe_ex2(int32_t blocks, int32_t iters, float* sink, attn_stream stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 ATTN_API int attn_version(void);
 

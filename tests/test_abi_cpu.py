@@ -145,8 +145,17 @@ def test_combine_checks(L):
     assert attn.attn_combine(4, 3, 64, FAKE, FAKE, 1, FAKE + 1, 64, None, 0, None) == attn.ATTN_ERR_ALIGNMENT
 
 
+def test_probe_checks(L):
+    """The exponential probe rejects its bad arguments before any launch."""
+    E = attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_probe_ex2(0, 1, FAKE, None) == E
+    assert attn.attn_probe_ex2(1, 0, FAKE, None) == E
+    assert attn.attn_probe_ex2(1, 1, None, None) == E
+    assert attn.attn_probe_ex2(1, 1, FAKE + 2, None) == E
+
+
 def test_status_strings_and_version(L):
     for code in range(7):
         assert attn.status_string(code) and attn.status_string(code) != "unknown status"
     assert attn.status_string(99) == "unknown status"
-    assert attn.attn_version() >= 220
+    assert attn.attn_version() >= 230

@@ -488,3 +488,15 @@ def test_decode_with_cache_append(i):
     ref_o, ref_l = oracle.attn(c.problem, c.q, k2, v2, k_lens=stored, k_scale=c.k_scale, v_scale=c.v_scale)
     compare(o, lse, ref_o.reshape(o.shape), ref_l.reshape(lse.shape), dtype, "nan", f"append{i}")
     assert attn.attn_device_status() == attn.ATTN_OK
+
+
+def test_ex2_probe_runs_and_keeps_its_chains_bounded():
+    """The exponential-throughput probe: every chain x <- -2^x stays in
+    [-1, -0.5], so each CTA's sum of 256 threads x 8 chains lies in
+    [-2048, -1024]."""
+    torch = torch_mod()
+    sink = torch.full((8,), float("nan"), dtype=torch.float32, device="cuda")
+    assert attn.attn_probe_ex2(8, 64, sink.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    s = sink.cpu().numpy()
+    assert np.all(np.isfinite(s)) and np.all(s >= -2048.0) and np.all(s <= -1024.0)
