@@ -338,73 +338,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_after();
       const int k0 = (j0 + i) * BN;
-      if (explicit_x) {
-        // Scores to log2 units with the additive mask, one 32-column chunk at a
-        // time (the wait's memory clobber keeps at most 32 mask loads live).
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          tmem_ld32(s_tm + c * 32, x + c * 32);
-          tmem_ld_wait_regs<1>(x + c * 32);
-#pragma unroll
-          for (int e = c * 32; e < c * 32 + 32; ++e) {
-            const int kk = k0 + e;
-            float v = -INFINITY;
-            if (kk >= lo && kk < hi) {
-              const float s = __uint_as_float(x[e]);
-              const float t = capped ? cap2 * tanh_exp2(s * kinv) : s * sc;
-              v = MASK ? fmaf(mrow[kk], kLog2e, t) : t;
-            }
-            x[e] = __float_as_uint(v);
-            if ((e & 7) == 7) asm volatile("" ::: "memory");  // at most 8 mask loads in flight
-          }
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
-        tmem_ld_wait_regs<BN / 32>(x);
-        if (!(k0 >= lo && k0 + BN <= hi)) {
-#pragma unroll
-          for (int e = 0; e < BN; ++e) {
-            const int kk = k0 + e;
-            if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
-          }
-        }
-      }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < BN; e += 4) {
-        mx0 = max3(mx0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-        mx1 = max3(mx1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
-      }
-      const float mt = fmaxf(mx0, mx1) * c_eff;
-      const bool raise = mt > m_ref + kSlack;     // also true for the first tile with a visible key
+      // With a finite reference maximum the tile's P is computed against it
+      // directly, without scanning for the tile maximum; a row whose tile sum
+      // reaches kLagMax (so some score rose that far above the reference) makes
+      // the warp redo the tile with the scan.  Below that bound P keeps its
+      // relative precision in its own type (bf16 up to 2^127, f16 up to 65504)
+      // and in the f32 sums, so only overflow needs the scan.
+      constexpr float kLagMax = BF16 ? 0x1p64f : 0x1p15f;
+      bool scan = __any_sync(0xffffffffu, !(m_ref > -INFINITY));
+      bool rescale = false;
       float corr = 1.f;
-      if (raise) corr = ex2(m_ref - mt);          // 0 when m_ref = -inf
-      // O holds earlier tiles' sums only if m_ref was finite; it is rescaled
-      // below, after P is stored (warp-uniform TMEM traffic).
-      const bool rescale = raise && m_ref > -INFINITY;
-      if (raise) {
-        l *= corr;
-        m_ref = mt;
-      }
-      const float neg = -(m_ref == -INFINITY ? 0.f : m_ref);
-      const uint64_t c2 = f2u(c_eff, c_eff), n2 = f2u(neg, neg);
-      float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        if (explicit_x) {
+          // Scores to log2 units with the additive mask, one 32-column chunk at a
+          // time (the wait's memory clobber keeps at most 32 mask loads live).
 #pragma unroll
-      for (int e = 0; e < BN; e += 4) {
-        float a0, a1, b0, b1;
-        fma2(a0, a1, __uint_as_float(x[e]), __uint_as_float(x[e + 1]), c2, n2);
-        fma2(b0, b1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]), c2, n2);
-        a0 = ex2(a0);
-        a1 = ex2(a1);
-        b0 = ex2(b0);
-        b1 = ex2(b1);
-        add2(la0, la1, a0, a1);
-        add2(lb0, lb1, b0, b1);
-        x[e / 2] = pack2<BF16>(a0, a1);
-        x[e / 2 + 1] = pack2<BF16>(b0, b1);
+          for (int c = 0; c < BN / 32; ++c) {
+            tmem_ld32(s_tm + c * 32, x + c * 32);
+            tmem_ld_wait_regs<1>(x + c * 32);
+#pragma unroll
+            for (int e = c * 32; e < c * 32 + 32; ++e) {
+              const int kk = k0 + e;
+              float v = -INFINITY;
+              if (kk >= lo && kk < hi) {
+                const float s = __uint_as_float(x[e]);
+                const float t = capped ? cap2 * tanh_exp2(s * kinv) : s * sc;
+                v = MASK ? fmaf(mrow[kk], kLog2e, t) : t;
+              }
+              x[e] = __float_as_uint(v);
+              if ((e & 7) == 7) asm volatile("" ::: "memory");  // at most 8 mask loads in flight
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
+          tmem_ld_wait_regs<BN / 32>(x);
+          if (!(k0 >= lo && k0 + BN <= hi)) {
+#pragma unroll
+            for (int e = 0; e < BN; ++e) {
+              const int kk = k0 + e;
+              if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
+            }
+          }
+        }
+        if (scan) {
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < BN; e += 4) {
+            mx0 = max3(mx0, __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+            mx1 = max3(mx1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]));
+          }
+          const float mt = fmaxf(mx0, mx1) * c_eff;
+          const bool raise = mt > m_ref + kSlack;     // also true for the first tile with a visible key
+          if (raise) corr = ex2(m_ref - mt);          // 0 when m_ref = -inf
+          // O holds earlier tiles' sums only if m_ref was finite; it is rescaled
+          // below, after P is stored (warp-uniform TMEM traffic).
+          rescale = raise && m_ref > -INFINITY;
+          if (raise) {
+            l *= corr;
+            m_ref = mt;
+          }
+        }
+        const float neg = -(m_ref == -INFINITY ? 0.f : m_ref);
+        const uint64_t c2 = f2u(c_eff, c_eff), n2 = f2u(neg, neg);
+        float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < BN; e += 4) {
+          float a0, a1, b0, b1;
+          fma2(a0, a1, __uint_as_float(x[e]), __uint_as_float(x[e + 1]), c2, n2);
+          fma2(b0, b1, __uint_as_float(x[e + 2]), __uint_as_float(x[e + 3]), c2, n2);
+          a0 = ex2(a0);
+          a1 = ex2(a1);
+          b0 = ex2(b0);
+          b1 = ex2(b1);
+          add2(la0, la1, a0, a1);
+          add2(lb0, lb1, b0, b1);
+          x[e / 2] = pack2<BF16>(a0, a1);
+          x[e / 2 + 1] = pack2<BF16>(b0, b1);
+        }
+        const float lt = (la0 + la1) + (lb0 + lb1);
+        if (scan || !__any_sync(0xffffffffu, lt >= kLagMax)) {   // NaN sums stay (a NaN row)
+          l += lt;
+          break;
+        }
+        scan = true;
       }
-      l += (la0 + la1) + (lb0 + lb1);
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) tmem_st32(s_tm + c * 32, x + c * 32);
       if (__any_sync(0xffffffffu, rescale)) {

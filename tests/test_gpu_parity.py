@@ -500,3 +500,24 @@ def test_ex2_probe_runs_and_keeps_its_chains_bounded():
     torch.cuda.synchronize()
     s = sink.cpu().numpy()
     assert np.all(np.isfinite(s)) and np.all(s >= -2048.0) and np.all(s <= -1024.0)
+
+
+@pytest.mark.parametrize("D,dtype,causal", [(128, "bf16", False), (128, "f16", True), (64, "bf16", True)])
+def test_scores_rising_far_above_the_reference_maximum(D, dtype, causal):
+    """Scores that jump well above a row's reference maximum after its first
+    key tiles: by 43 log2 units (P up to 2^43 in bf16 kept without a rescale; in
+    f16, past 2^15, the tile is redone), by 87
+    and 88 (the tile is redone with its maximum), and to +inf at one key (a
+    NaN row).  All against the oracle."""
+    B, H, Sq, Sk = 3, 4, 256, 640
+    r = np.random.default_rng(77 + D)
+    mask = (r.standard_normal((B, 1, 1, Sk)) * 0.5).astype(np.float32)
+    mask[0, 0, 0, 200:] += 30.0
+    mask[1, 0, 0, 300:] += 60.0
+    mask[1, 0, 0, 500:] += 1.0
+    mask[2, 0, 0, 150:] += 20.0
+    mask[2, 0, 0, 400] = np.inf
+    c = wl.make_case(name=f"rise{D}", seed=88, dtype=dtype, batch=B, heads=H, q_len=Sq, k_len=Sk, head_dim=D,
+                     causal=causal, causal_offset=Sk - Sq if causal else None, mask=mask)
+    st, _ = run_and_compare(c)
+    assert st["nan_rows"] == H * (Sq if not causal else Sq - (400 - (Sk - Sq)))
