@@ -138,20 +138,23 @@ int check_pointers(const attn_problem* p, const void* q, const void* k, const vo
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// Decode key-range plan: depends only on the shape.  Ranges are a multiple
-// of 32 keys, at least 128 keys, at most 16 of them ("Attention", section
-// "Accuracy at long key lengths"); a range of 512 keys or more is kept
-// whole when the (batch, kv head) pairs alone fill the GPU several times.
+// Decode key-range plan: depends only on the shape ("Attention", section
+// "Accuracy at long key lengths": ranges cut by the shape, merged in range
+// order).  Ranges are a multiple of 32 keys, at least 128 keys, at most 8 of
+// them a row: each range pays a fixed cost (its CTA's pipeline fill, Q load,
+// four-warp merge and partial write), and on GB300 ranges of an eighth of
+// the cache measured faster than sixteenths (the tail of unequal ranges
+// grows less than the fixed costs shrink) and far faster than 32nds.
 //
-// int8 caches carry half the bytes per key, so a range's fixed costs (Q
-// load and scaling, the four-warp merge, the partial write) weigh twice as
-// much: their plan targets about 2048 ranges in all over (batch, kv head)
-// pairs, at most 16 a row, each a multiple of the 64-key stage.
+// int8 caches carry half the bytes per key, so those fixed costs weigh twice
+// as much: their plan targets about 4096 ranges in all over (batch, kv head)
+// pairs, at most 16 a row, each a multiple of the 64-key stage (measured
+// against 2048, 8192 and 16384).
 void decode_plan(const attn_problem* p, int* n_splits, int* split_len) {
   const int64_t Sk = p->k_len > 0 ? p->k_len : 1;
   if (p->kv_dtype == ATTN_KV_INT8) {
     const int64_t pairs = (int64_t)(p->batch > 0 ? p->batch : 1) * p->kv_heads;
-    int64_t n = (2048 + pairs - 1) / pairs;
+    int64_t n = (4096 + pairs - 1) / pairs;
     n = n < 1 ? 1 : (n > 16 ? 16 : n);
     int64_t len = (Sk + n - 1) / n;
     len = (len + 63) / 64 * 64;
@@ -160,7 +163,7 @@ void decode_plan(const attn_problem* p, int* n_splits, int* split_len) {
     *n_splits = (int)((Sk + len - 1) / len);
     return;
   }
-  int64_t len = (Sk + 15) / 16;
+  int64_t len = (Sk + 7) / 8;
   len = (len + 31) / 32 * 32;
   if (len < 128) len = 128;
   if (len > Sk) len = (Sk + 31) / 32 * 32;

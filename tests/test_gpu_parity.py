@@ -521,3 +521,36 @@ def test_scores_rising_far_above_the_reference_maximum(D, dtype, causal):
                      causal=causal, causal_offset=Sk - Sq if causal else None, mask=mask)
     st, _ = run_and_compare(c)
     assert st["nan_rows"] == H * (Sq if not causal else Sq - (400 - (Sk - Sq)))
+
+
+MIXED = [
+    # dtype, B, H, G, cap, lens kind, extras
+    ("bf16", 37, 40, 2, 3000, "mixed", {}),                                   # 20 heads a group: two head blocks
+    ("f16", 200, 8, 8, 700, "short", {}),                                      # many short rows
+    ("bf16", 5, 32, 8, 9000, "mixed", dict(softcap=30.0, head_sink="heads")),  # transforms, long rows
+    ("bf16", 64, 16, 4, 1500, "zeros", {}),                                    # most entries without a key
+]
+
+
+@pytest.mark.parametrize("i", range(len(MIXED)))
+def test_decode_mixed_key_lengths(i):
+    """The tensor-core decode pass over batches whose entries hold zero, few and
+    many keys (empty ranges, ranges cut short, rows over many ranges), with
+    one or two blocks of query heads per kv head, against the oracle (O and
+    LSE)."""
+    dtype, B, H, G, cap, kind, extra = MIXED[i]
+    r = np.random.default_rng(1600 + i)
+    if kind == "mixed":
+        k_lens = r.integers(0, cap + 1, size=B)
+        k_lens[: max(1, B // 8)] = 0
+        k_lens[-1] = cap
+    elif kind == "short":
+        k_lens = r.integers(1, 200, size=B)
+    else:
+        k_lens = np.where(r.random(B) < 0.8, 0, r.integers(1, cap + 1, size=B))
+    extra = dict(extra)
+    if extra.get("head_sink") == "heads":
+        extra["head_sink"] = (r.standard_normal(H) * 2).astype(np.float32)
+    c = wl.make_case(name=f"bal{i}", seed=1700 + i, dtype=dtype, batch=B, heads=H, kv_heads=G, q_len=1, k_len=cap,
+                     head_dim=128, k_lens=k_lens.astype(np.int32), decode=True, **extra)
+    run_and_compare(c)
