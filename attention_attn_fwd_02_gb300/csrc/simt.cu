@@ -103,23 +103,38 @@ __global__ void __launch_bounds__(kThreads) simt_attn_kernel(Problem p, Split sp
 
   for (int t0 = (u_lo / kTile) * kTile; t0 < u_hi; t0 += kTile) {
     __syncthreads();
-    // Stage the tile; keys outside the CTA's union are zero (never read from memory).
-    for (int e = threadIdx.x; e < kTile * D; e += kThreads) {
-      const int j = e / D, d = e - j * D;
-      const int kk = t0 + j;
-      float kv = 0.f, vv = 0.f;
-      if (kk >= u_lo && kk < u_hi) {
-        if constexpr (KV8) {
-          const int si = p.kv_per_channel ? g * D + d : 0;
-          kv = (float)reinterpret_cast<const int8_t*>(p.K)[kb + (int64_t)kk * p.k.rs + d] * p.k_scale[si];
-          vv = (float)reinterpret_cast<const int8_t*>(p.V)[vb + (int64_t)kk * p.v.rs + d] * p.v_scale[si];
-        } else {
-          kv = to_f32(K[kb + (int64_t)kk * p.k.rs + d]);
-          vv = to_f32(V[vb + (int64_t)kk * p.v.rs + d]);
+    // Stage the tile; keys outside the CTA's union are zero (never read from
+    // memory).  Each thread issues the loads of kBatch elements before it
+    // stores any, so a tile costs about one memory latency, not kBatch.
+    constexpr int kBatch = 8;
+    for (int e0 = threadIdx.x; e0 < kTile * D; e0 += kThreads * kBatch) {
+      float kv[kBatch], vv[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kThreads;
+        const int j = e / D, d = e - j * D;
+        const int kk = t0 + j;
+        kv[u] = 0.f;
+        vv[u] = 0.f;
+        if (e < kTile * D && kk >= u_lo && kk < u_hi) {
+          if constexpr (KV8) {
+            const int si = p.kv_per_channel ? g * D + d : 0;
+            kv[u] = (float)reinterpret_cast<const int8_t*>(p.K)[kb + (int64_t)kk * p.k.rs + d] * p.k_scale[si];
+            vv[u] = (float)reinterpret_cast<const int8_t*>(p.V)[vb + (int64_t)kk * p.v.rs + d] * p.v_scale[si];
+          } else {
+            kv[u] = to_f32(K[kb + (int64_t)kk * p.k.rs + d]);
+            vv[u] = to_f32(V[vb + (int64_t)kk * p.v.rs + d]);
+          }
         }
       }
-      Ks[e] = kv;
-      Vs[e] = vv;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kThreads;
+        if (e < kTile * D) {
+          Ks[e] = kv[u];
+          Vs[e] = vv[u];
+        }
+      }
     }
     __syncthreads();
 
