@@ -224,21 +224,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q_addr = su32(q_s), k_addr = su32(k_s), v_addr = su32(v_s);
     bool ok = n_tiles > 0;
     if (ok) ok = wait_warp(&sb.q_full, 0, &sb.abort, p.status);
+    // Descriptors of each operand tile's start; the K-steps add constants.
+    const uint64_t qd0 = sdesc(q_addr, 16, 1024), qd1 = sdesc(q_addr + C::kQTile, 16, 1024);
+    const uint64_t kd0 = sdesc(k_addr, 16, 1024), vd0 = sdesc(v_addr, BN * 128, 1024);
     auto issue_qk = [&](int tt, int s) {
       fence_after();
+      const uint64_t ad = tt ? qd1 : qd0;
+      const uint64_t bd0 = sdesc_add(kd0, (uint32_t)(s * C::kKTile));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (uint32_t)((kk / 4) * BM * 128 + (kk % 4) * 32);
-        const uint64_t a = sdesc(q_addr + tt * C::kQTile + off, 16, 1024);
-        const uint64_t bd = sdesc(k_addr + s * C::kKTile + (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32), 16, 1024);
+        const uint64_t a = sdesc_add(ad, (uint32_t)((kk / 4) * BM * 128 + (kk % 4) * 32));
+        const uint64_t bd = sdesc_add(bd0, (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32));
         mma_ss(tmem + (tt ? C::kS1 : C::kS0), a, bd, kIdQK, kk > 0);
       }
     };
     auto issue_pv = [&](int tt, int s, bool first) {
       fence_after();
+      const uint64_t bd0 = sdesc_add(vd0, (uint32_t)(s * C::kKTile));
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t bd = sdesc(v_addr + s * C::kKTile + kk * 16 * 128, BN * 128, 1024);
+        const uint64_t bd = sdesc_add(bd0, (uint32_t)(kk * 16 * 128));
         mma_ts(tmem + (tt ? C::kO1 : C::kO0), tmem + (tt ? C::kS1 : C::kS0) + kk * 8, bd, kIdPV,
                (!first || kk > 0) ? 1u : 0u);
       }

@@ -233,6 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdQK = idesc_f16(BF16, false, BM, BN);
     constexpr uint32_t kIdPV = idesc_f16(BF16, true, BM, D);
     const uint32_t q_addr = su32(q_s), ring_addr = su32(ring);
+    // Descriptors of the operand tiles' starts; the K-steps add constants.
+    const uint64_t qd = sdesc(q_addr, 16, 1024), ud = sdesc(ring_addr, 16, 1024),
+                   vd = sdesc(ring_addr, (BN / 2) * 128, 1024);
     int taken = 0;  // units consumed so far (ring position)
     bool ok = n_tiles > 0;
     // Waits for the next unit; returns its shared address (0 on abort).
@@ -255,11 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ku) return false;
         if (lane == 0) {
           fence_after();
+          const uint64_t bd0 = sdesc_add(ud, ku - ring_addr);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const int kq = hf * 8 + kk;  // K-step over head_dim
-            const uint64_t a = sdesc(q_addr + (uint32_t)((kq / 4) * BM * 128 + (kq % 4) * 32), 16, 1024);
-            const uint64_t bd = sdesc(ku + (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32), 16, 1024);
+            const uint64_t a = sdesc_add(qd, (uint32_t)((kq / 4) * BM * 128 + (kq % 4) * 32));
+            const uint64_t bd = sdesc_add(bd0, (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32));
             mma_ss(tmem + (slot ? C::kS1 : C::kS0), a, bd, kIdQK, kq > 0);
           }
         }
@@ -292,9 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           fence_after();
+          const uint64_t bd0 = sdesc_add(vd, vu - ring_addr);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc(vu + (uint32_t)(kk * 16 * 128), (BN / 2) * 128, 1024);
+            const uint64_t bd = sdesc_add(bd0, (uint32_t)(kk * 16 * 128));
             mma_ts(tmem + C::kO, tmem + (slot ? C::kS1 : C::kS0) + (hf * 4 + kk) * 8, bd, kIdPV,
                    (!first || hf > 0 || kk > 0) ? 1u : 0u);
           }

@@ -176,6 +176,17 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;
 }
 
+// The descriptor of the operand `bytes` further on (a multiple of 16): the
+// start address is the low 14 bits in 16-byte units and every shared address
+// of a CTA stays below 256 KB, so a 32-bit add on the low word cannot carry
+// out of that field.  One add per MMA instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = (uint32_t)d + (bytes >> 4), hi = (uint32_t)(d >> 32);
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
 // Instruction descriptor, kind::f16 with f32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int M, int N) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
