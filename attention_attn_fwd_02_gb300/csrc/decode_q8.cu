@@ -40,8 +40,10 @@
 //
 // CTA: 4 warps; one (batch, kv head, key range) and up to 8 (or 16, two MMA
 // column tiles) query heads of that kv head, so each cache byte is read once.
-// The range streams through shared memory in 64-key stages, three deep
-// (48 KB), copied by TMA with 128-byte swizzle (conflict-free ldmatrix);
+// The range streams through shared memory in 64-key stages, two deep (32 KB,
+// so five CTAs share an SM at 96 registers a thread: more resident warps beat
+// a deeper ring here, measured against three and four stages), copied by TMA
+// with 128-byte swizzle (conflict-free ldmatrix);
 // warp w takes keys 16w .. 16w+15 of a stage.  Waits are bounded (status word
 // on timeout).
 #include <stdlib.h>
@@ -67,7 +69,7 @@ constexpr int kD = 128;
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStageKeys = 64;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kTile = kStageKeys * kD;   // bytes of the K (or V) tile of a stage
 constexpr float kBias = 1152.f;          // the f16 value of a biased int8 0
 constexpr float kLog2e = 1.4426950408889634f;
