@@ -13,8 +13,10 @@
 //
 // One CTA (4 warps) owns one (batch, kv head, key range) and up to 16 query
 // heads of that kv head, so each cache byte is read once.  The range streams
-// through shared memory in 64-key stages, three deep, copied by TMA with
-// 128-byte swizzle; warp w takes keys 16w..16w+15 of a stage.  The per-group
+// through shared memory in 64-key stages, two deep (64 KB, so three CTAs
+// share an SM: more resident warps beat a deeper ring, measured against three
+// and four stages), copied by TMA with 128-byte swizzle; warp w takes keys
+// 16w..16w+15 of a stage.  The per-group
 // contractions run on the tensor cores with mma.sync (m16n8k16, f32
 // accumulation) only to keep instruction issue far below the HBM rate: with
 // the CTA's query heads as the 16 MMA rows (zero-padded), S[head][key] = Q K^T
@@ -114,7 +116,7 @@ __device__ __forceinline__ float ex2(float x) {
 // accumulator layout is the P operand layout, so P never leaves registers.
 
 constexpr int kMStageKeys = 64;
-constexpr int kMStages = 3;
+constexpr int kMStages = 2;
 constexpr int kMTile = kMStageKeys * kRowBytes;  // K or V tile of a stage (two 64-column chunks)
 constexpr int kMHeads = 16;                      // query heads per CTA (MMA rows)
 
