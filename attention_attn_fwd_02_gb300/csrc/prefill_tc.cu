@@ -105,18 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = h / p.qpg;
   const int q0 = qb * 2 * BM;
 
-  // ---- row ranges and their union ----
-  const int t = warp / 4;                       // query tile of a softmax thread
-  const int r = (warp % 4) * 32 + lane;         // row within the tile = TMEM lane
-  const int qrow = q0 + t * BM + r;
-  int lo = 0, hi = 0;
-  if (warp < 8 && qrow < p.Sq) {
-    int64_t lo64, hi64;
-    row_range(p, b, qrow, lo64, hi64);
-    lo = (int)lo64;
-    hi = (int)(hi64 > lo64 ? hi64 : lo64);
-  }
   if (threadIdx.x == 0) {
+    // The copies' descriptors start on their way before anything else.
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
     sb.lo_u = 0x7fffffff;
     sb.hi_u = -1;
     sb.abort = 0;
@@ -134,6 +127,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sb.mma_done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // Q does not depend on the key range: its copy starts at once.
+    mbar_expect_tx(&sb.q_full, 2 * C::kQTile);
+    for (int tt = 0; tt < 2; ++tt)
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
+  }
+  // ---- row ranges and their union ----
+  const int t = warp / 4;                       // query tile of a softmax thread
+  const int r = (warp % 4) * 32 + lane;         // row within the tile = TMEM lane
+  const int qrow = q0 + t * BM + r;
+  int lo = 0, hi = 0;
+  if (warp < 8 && qrow < p.Sq) {
+    int64_t lo64, hi64;
+    row_range(p, b, qrow, lo64, hi64);
+    lo = (int)lo64;
+    hi = (int)(hi64 > lo64 ? hi64 : lo64);
   }
   if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&sb.tmem_base))
@@ -143,13 +152,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before();
   __syncthreads();
   fence_after();
-  // Q does not depend on the key range: its copy starts at once.
-  if (threadIdx.x == 8 * 32) {
-    mbar_expect_tx(&sb.q_full, 2 * C::kQTile);
-    for (int tt = 0; tt < 2; ++tt)
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
-  }
   // The union of the rows' visible key ranges.  Without segment starts both
   // ends of a row's range are non-decreasing in the row (the window's left end
   // moves with the diagonal), so [lo of the first row, hi of the last row)

@@ -147,17 +147,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = h / p.qpg;
   const int q0 = qb * BM;
 
-  const int r = (warp % 4) * 32 + lane;  // softmax row = TMEM lane (warps 0-7)
-  const int ch = warp / 4;                // key half / O half of a softmax thread
-  const int qrow = q0 + r;
-  int lo = 0, hi = 0;
-  if (warp < 8 && qrow < p.Sq) {
-    int64_t lo64, hi64;
-    row_range(p, b, qrow, lo64, hi64);
-    lo = (int)lo64;
-    hi = (int)(hi64 > lo64 ? hi64 : lo64);
-  }
   if (threadIdx.x == 0) {
+    // The copies' descriptors start on their way before anything else.
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
     sb.lo_u = 0x7fffffff;
     sb.hi_u = -1;
     sb.abort = 0;
@@ -174,6 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sb.mma_done, 1);
     for (int w = 0; w < 4; ++w) mbar_init(&sb.pair[w], 64);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // Q does not depend on the key range: its copy starts at once.
+    mbar_expect_tx(&sb.q_full, C::kQTile);
+    for (int c = 0; c < D / 64; ++c) tma_load_4d(q_s + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0, h, b);
+  }
+  const int r = (warp % 4) * 32 + lane;  // softmax row = TMEM lane (warps 0-7)
+  const int ch = warp / 4;                // key half / O half of a softmax thread
+  const int qrow = q0 + r;
+  int lo = 0, hi = 0;
+  if (warp < 8 && qrow < p.Sq) {
+    int64_t lo64, hi64;
+    row_range(p, b, qrow, lo64, hi64);
+    lo = (int)lo64;
+    hi = (int)(hi64 > lo64 ? hi64 : lo64);
   }
   if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&sb.tmem_base))
@@ -183,11 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before();
   __syncthreads();
   fence_after();
-  // Q does not depend on the key range: its copy starts at once.
-  if (threadIdx.x == 8 * 32) {
-    mbar_expect_tx(&sb.q_full, C::kQTile);
-    for (int c = 0; c < D / 64; ++c) tma_load_4d(q_s + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0, h, b);
-  }
   if (warp < 4 && hi > lo) {   // the rows' ranges (warps 4-7 hold the same rows)
     atomicMin(&sb.lo_u, lo);
     atomicMax(&sb.hi_u, hi);

@@ -80,6 +80,11 @@ __device__ __forceinline__ bool wait_warp(uint64_t* b, uint32_t parity, int* abo
   return __all_sync(0xffffffffu, ok);
 }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter) ahead of its first copy.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
                                             int c3) {
   asm volatile(
