@@ -255,6 +255,14 @@ def long_causal_gqa_bf16(seed: int = 3, batch: int = 2, seq: int = 4096, heads: 
                      k_lens=k_lens)
 
 
+def dense_gqa_bf16(seed: int = 3, batch: int = 2, seq: int = 4096, heads: int = 32, kv_heads: int = 8) -> Case:
+    """The long GQA prefill's shape without the causal bound or key lengths: every query sees every key
+    (a context measurement of the tensor-core kernel's steady state)."""
+    return make_case(name=f"dense_gqa_bf16_b{batch}_h{heads}_kv{kv_heads}_s{seq}_d128", seed=seed, dtype="bf16",
+                     layout="bhsd", batch=batch, heads=heads, kv_heads=kv_heads, q_len=seq, head_dim=128,
+                     causal=False, causal_offset=None, value_scale=0.5)
+
+
 def decode_bnsh_bf16(seed: int = 4, batch: int = 64, capacity: int = 8192, heads: int = 32,
                      kv_heads: int = 8, min_len: int = 512) -> Case:
     """Batched single-query decode over a BNSH cache [B, 8, capacity, 128], lengths uniform in [512, capacity]."""
