@@ -44,6 +44,8 @@ FULL = {
     "decode_bnsh_bf16": lambda: wl.decode_bnsh_bf16(),
     "cross_mask_f16_nan": lambda: wl.cross_mask_f16(masked_rows="nan"),
     "cross_mask_f16_zero": lambda: wl.cross_mask_f16(masked_rows="zero"),
+    "decode_bnsh_int8": lambda: wl.decode_bnsh_int8(),
+    "dense_gqa_bf16": lambda: wl.dense_gqa_bf16(),
 }
 
 
@@ -56,7 +58,8 @@ def test_full_size_sampled_rows(name):
     assert attn.attn_device_status() == attn.ATTN_OK
     rows = sample_rows(case)
     ref_o, ref_l = oracle.attn(case.problem, case.q, case.k, case.v, mask=case.mask, seg=case.seg,
-                               k_lens=case.k_lens, rows=rows)
+                               k_lens=case.k_lens, rows=rows, head_sink=case.head_sink,
+                               k_scale=case.k_scale, v_scale=case.v_scale)
     got_o = o[rows[:, 0], rows[:, 1], rows[:, 2]]
     got_l = lse[rows[:, 0], rows[:, 1], rows[:, 2]]
     compare(got_o, got_l, ref_o, ref_l, case.problem["dtype"], case.problem["masked_rows"], name)
