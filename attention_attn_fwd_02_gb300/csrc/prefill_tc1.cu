@@ -346,8 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Soft-capping: the scaled product s becomes cap2 * tanh(s_raw * kinv) in log2 units.
     const bool capped = p.softcap > 0.f;
     const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
-    const bool explicit_x = MASK || !(sc > 0.f) || capped;
-    const float c_eff = explicit_x ? 1.f : sc;
+    // With a mask, no softcap and a positive scale the scores stay in natural
+    // units, s * scale + mask (one packed FMA for two keys), and the exponent's
+    // multiplier takes log2(e); other transformed scores are formed in log2 units.
+    const bool mask_nat = MASK && !capped && sc > 0.f;
+    const bool explicit_x = (MASK && !mask_nat) || !(sc > 0.f) || capped;
+    const float c_eff = mask_nat ? kLog2e : (explicit_x ? 1.f : sc);
+    const uint64_t scale2 = f2u(p.scale, p.scale);
     const float* mrow = nullptr;
     if (MASK && qrow < p.Sq)
       mrow = p.M + p.m.off + (int64_t)b * p.m.bs + (int64_t)h * p.m.hs + (int64_t)qrow * p.m.rs;
@@ -386,7 +391,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(s_tm + ch * kHalf, x);
       tmem_ld32(s_tm + ch * kHalf + 32, x + 32);
       tmem_ld_wait_regs<2>(x);
-      if (explicit_x) {
+      const bool inside = k0 >= lo && k0 + kHalf <= hi;
+      if (mask_nat) {
+#pragma unroll
+        for (int e = 0; e < kHalf; e += 2) {
+          float v0, v1;
+          fma2(v0, v1, __uint_as_float(x[e]), __uint_as_float(x[e + 1]), scale2, f2u(mv[e], mv[e + 1]));
+          x[e] = __float_as_uint(v0);
+          x[e + 1] = __float_as_uint(v1);
+        }
+        if (!inside) {
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) {
+            const int kk = k0 + e;
+            if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
+          }
+        }
+      } else if (explicit_x) {
         // Scores to log2 units plus the additive mask.
 #pragma unroll
         for (int e = 0; e < kHalf; ++e) {
@@ -396,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float v = MASK ? fmaf(mv[e], kLog2e, t) : t;
           x[e] = __float_as_uint((kk >= lo && kk < hi) ? v : -INFINITY);
         }
-      } else if (!(k0 >= lo && k0 + kHalf <= hi)) {
+      } else if (!inside) {
 #pragma unroll
         for (int e = 0; e < kHalf; ++e) {
           const int kk = k0 + e;
