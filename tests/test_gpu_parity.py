@@ -502,7 +502,8 @@ def test_ex2_probe_runs_and_keeps_its_chains_bounded():
     assert np.all(np.isfinite(s)) and np.all(s >= -2048.0) and np.all(s <= -1024.0)
 
 
-@pytest.mark.parametrize("D,dtype,causal", [(128, "bf16", False), (128, "f16", True), (64, "bf16", True)])
+@pytest.mark.parametrize("D,dtype,causal", [(128, "bf16", False), (128, "f16", True), (64, "bf16", True),
+                                             (256, "f16", False), (256, "bf16", True)])
 def test_scores_rising_far_above_the_reference_maximum(D, dtype, causal):
     """Scores that jump well above a row's reference maximum after its first
     key tiles: by 43 log2 units (P up to 2^43 in bf16 kept without a rescale; in
