@@ -330,8 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Soft-capping: the scaled product s becomes cap2 * tanh(s_raw * kinv) in log2 units.
     const bool capped = p.softcap > 0.f;
     const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
-    const bool explicit_x = MASK || !(sc > 0.f) || capped;
-    const float c_eff = explicit_x ? 1.f : sc;
+    // With a mask, no softcap and a positive scale the scores stay in natural
+    // units, s * scale + mask (one packed FMA for two keys, the mask read as
+    // float4 where it can be), and the exponent's multiplier takes log2(e);
+    // other transformed scores are formed in log2 units.
+    const bool mask_nat = MASK && !capped && sc > 0.f;
+    const bool explicit_x = (MASK && !mask_nat) || !(sc > 0.f) || capped;
+    const float c_eff = mask_nat ? kLog2e : (explicit_x ? 1.f : sc);
+    const uint64_t scale2 = f2u(p.scale, p.scale);
     const float* mrow = nullptr;
     if (MASK && qrow < p.Sq)
       mrow = p.M + p.m.off + (int64_t)b * p.m.bs + (int64_t)h * p.m.hs + (int64_t)qrow * p.m.rs;
@@ -357,7 +363,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       float corr = 1.f;
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
-        if (explicit_x) {
+        if (mask_nat) {
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            tmem_ld32(s_tm + c * 32, x + c * 32);
+            tmem_ld_wait_regs<1>(x + c * 32);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {   // 16 keys at a time keeps few mask values live
+              float mv[16];
+              const int kc = k0 + c * 32 + hf * 16;
+              const float* mp = mrow ? mrow + kc : nullptr;
+              if (mp && kc >= lo && kc + 16 <= hi && ((uintptr_t)mp & 15) == 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
+                  mv[4 * j] = v4.x;
+                  mv[4 * j + 1] = v4.y;
+                  mv[4 * j + 2] = v4.z;
+                  mv[4 * j + 3] = v4.w;
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) mv[e] = (mp && kc + e >= lo && kc + e < hi) ? mp[e] : 0.f;
+              }
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                const int xe = c * 32 + hf * 16 + e;
+                float v0, v1;
+                fma2(v0, v1, __uint_as_float(x[xe]), __uint_as_float(x[xe + 1]), scale2, f2u(mv[e], mv[e + 1]));
+                x[xe] = __float_as_uint(v0);
+                x[xe + 1] = __float_as_uint(v1);
+              }
+            }
+          }
+          if (!(k0 >= lo && k0 + BN <= hi)) {
+#pragma unroll
+            for (int e = 0; e < BN; ++e) {
+              const int kk = k0 + e;
+              if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
+            }
+          }
+        } else if (explicit_x) {
           // Scores to log2 units with the additive mask, one 32-column chunk at a
           // time (the wait's memory clobber keeps at most 32 mask loads live).
 #pragma unroll

@@ -263,6 +263,18 @@ def dense_gqa_bf16(seed: int = 3, batch: int = 2, seq: int = 4096, heads: int = 
                      causal=False, causal_offset=None, value_scale=0.5)
 
 
+def masked_gqa_bf16(seed: int = 3, batch: int = 2, seq: int = 4096, heads: int = 32, kv_heads: int = 8) -> Case:
+    """The long GQA prefill's shapes with a float32 padding mask [B,1,1,K] instead of the causal bound:
+    N(0,1) values, the last key_len/8 keys of each batch entry -inf (a context measurement of the masked
+    score path)."""
+    r = rng(seed, MASK_ID)
+    mask = r.standard_normal((batch, 1, 1, seq)).astype(np.float32)
+    mask[:, :, :, seq - seq // 8:] = -np.inf
+    return make_case(name=f"masked_gqa_bf16_b{batch}_h{heads}_kv{kv_heads}_s{seq}_d128", seed=seed, dtype="bf16",
+                     layout="bhsd", batch=batch, heads=heads, kv_heads=kv_heads, q_len=seq, head_dim=128,
+                     causal=False, causal_offset=None, value_scale=0.5, mask=mask, mask_kind="b11k")
+
+
 def decode_bnsh_bf16(seed: int = 4, batch: int = 64, capacity: int = 8192, heads: int = 32,
                      kv_heads: int = 8, min_len: int = 512) -> Case:
     """Batched single-query decode over a BNSH cache [B, 8, capacity, 128], lengths uniform in [512, capacity]."""

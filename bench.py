@@ -514,6 +514,7 @@ CASES = {
     "gqa_doc_causal_bf16": lambda: wl.gqa_doc_causal_bf16(),
     "long_causal_gqa_bf16": lambda: wl.long_causal_gqa_bf16(),
     "dense_gqa_bf16": lambda: wl.dense_gqa_bf16(),
+    "masked_gqa_bf16": lambda: wl.masked_gqa_bf16(),
     "decode_bnsh_bf16": lambda: wl.decode_bnsh_bf16(),
     "decode_bnsh_int8": lambda: wl.decode_bnsh_int8(),
     "cross_mask_f16": lambda: wl.cross_mask_f16(),
