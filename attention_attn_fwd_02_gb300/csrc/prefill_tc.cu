@@ -75,7 +75,8 @@ struct Cfg {
   static constexpr int kStages = D <= 64 ? 4 : 2;
   static constexpr int kQTile = BM * D * 2;               // bytes
   static constexpr int kKTile = BN * D * 2;
-  static constexpr int kSmem = 2 * kQTile + 2 * kStages * kKTile;
+  static constexpr int kMaskTile = BN * 4;                // a key tile's broadcast mask values (f32)
+  static constexpr int kSmem = 2 * kQTile + 2 * kStages * kKTile + kStages * kMaskTile;
   static constexpr int kS0 = 0, kS1 = BN, kO0 = 2 * BN, kO1 = 2 * BN + D;
   static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
 };
@@ -83,13 +84,17 @@ struct Cfg {
 template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks) {
+                      const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
+                      const int mask_bcast) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;
   uint8_t* k_s = q_s + 2 * C::kQTile;
   uint8_t* v_s = k_s + C::kStages * C::kKTile;
+  // A mask broadcast over heads and rows ([B,1,1,K], 16-byte aligned) is staged
+  // per key tile with the V copy and read from here by every softmax thread.
+  float* m_s = reinterpret_cast<float*>(v_s + C::kStages * C::kKTile);
   __shared__ Bars sb;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -201,7 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           k_only = i;
           break;
         }
-        mbar_expect_tx(&sb.v_full[s], C::kKTile);
+        const uint32_t mbytes = MASK && mask_bcast ? (uint32_t)min(BN, p.Sk - krow) * 4u : 0u;
+        mbar_expect_tx(&sb.v_full[s], C::kKTile + mbytes);
+        if (mbytes)
+          bulk_load(m_s + s * BN, p.M + p.m.off + (int64_t)b * p.m.bs + krow, mbytes, &sb.v_full[s]);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(v_s + s * C::kKTile + c * BN * 128, &tm_v, &sb.v_full[s], c * 64, krow, g, b);
         issued = i + 1;
@@ -349,8 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
+      // The staged mask values arrive with V(i); its stage is freed only after
+      // P V(i), so they stay in place while this tile's softmax reads them.
+      if (MASK && mask_bcast &&
+          !wait_warp(&sb.v_full[i % C::kStages], (uint32_t)(i / C::kStages) & 1u, &sb.abort, p.status)) {
+        ok = false;
+        break;
+      }
       fence_after();
       const int k0 = (j0 + i) * BN;
+      const float* ms = m_s + (i % C::kStages) * BN;   // staged mask values of this key tile
       // With a finite reference maximum the tile's P is computed against it
       // directly, without scanning for the tile maximum; a row whose tile sum
       // reaches kLagMax (so some score rose that far above the reference) makes
@@ -373,7 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               float mv[16];
               const int kc = k0 + c * 32 + hf * 16;
               const float* mp = mrow ? mrow + kc : nullptr;
-              if (mp && kc >= lo && kc + 16 <= hi && ((uintptr_t)mp & 15) == 0) {
+              if (mask_bcast) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) mv[e] = ms[c * 32 + hf * 16 + e];   // out-of-range keys are hidden below
+              } else if (mp && kc >= lo && kc + 16 <= hi && ((uintptr_t)mp & 15) == 0) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
@@ -576,7 +595,14 @@ int launch(const Problem& p, cudaStream_t st) {
   if (!regs_ok) return -1;
   cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb);
+  // Broadcast mask rows are copied in bulk: 16-byte aligned rows and tiles
+  // whose byte counts are multiples of 16 (key tiles start at multiples of
+  // BN, so k_len divisible by 4 suffices).
+  const int mask_bcast = (MASK && p.m.hs == 0 && p.m.rs == 0 && p.m.off % 4 == 0 && p.m.bs % 4 == 0 &&
+                          (reinterpret_cast<uintptr_t>(p.M) & 15) == 0 && p.Sk % 4 == 0)
+                             ? 1
+                             : 0;
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, mask_bcast);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

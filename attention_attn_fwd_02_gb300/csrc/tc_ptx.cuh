@@ -80,6 +80,15 @@ __device__ __forceinline__ bool wait_warp(uint64_t* b, uint32_t parity, int* abo
   return __all_sync(0xffffffffu, ok);
 }
 
+// Contiguous bulk copy global -> shared, completing on `bar` (both addresses
+// 16-byte aligned, `bytes` a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   su32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(su32(bar))
+               : "memory");
+}
+
 // Fetch a tensor map (a __grid_constant__ kernel parameter) ahead of its first copy.
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
