@@ -137,6 +137,43 @@ def test_decode_checks(L):
                             None) == attn.ATTN_ERR_ALIGNMENT
 
 
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def _plan(k_len, pairs, int8):
+    """The decode key-range plan as the header and its comments state it: at most 8
+    ranges a row (multiples of 32 keys, at least 128, no longer than the cache rounded
+    up); for int8 caches ~4096 ranges over the (batch, kv head) pairs, at most 16 a
+    row, multiples of 64 keys, at least 128."""
+    if int8:
+        n = min(16, max(1, -(-4096 // pairs)))
+        length = max(128, -(-(-(-k_len // n)) // 64) * 64)
+        return -(-k_len // length)
+    length = -(-k_len // 8)
+    length = max(128, -(-length // 32) * 32)
+    if length > k_len:
+        length = -(-k_len // 32) * 32
+    return -(-k_len // length)
+
+
+@pytest.mark.parametrize("k_len,batch,kv_heads,int8", [
+    (8192, 64, 8, False), (3000, 4, 2, False), (100, 2, 2, False), (1, 1, 1, False),
+    (8192, 64, 8, True), (3000, 4, 2, True), (700, 200, 8, True), (100, 2, 2, True)])
+def test_decode_workspace_follows_the_range_plan(L, k_len, batch, kv_heads, int8):
+    """The workspace holds one partial (head_dim floats) and one LSE per (batch,
+    head, range); the range count follows the shape-only plan."""
+    heads, D = 4 * kv_heads, 128
+    kw = dict(batch=batch, heads=heads, kv_heads=kv_heads, q_len=1, k_len=k_len, head_dim=D,
+              q_layout=(0, heads * D, D, D), o_layout=(0, heads * D, D, D),
+              k_layout=(0, kv_heads * k_len * D, k_len * D, D), v_layout=(0, kv_heads * k_len * D, k_len * D, D))
+    if int8:
+        kw.update(kv_dtype="i8", kv_scale="channel", k_scale_ptr=FAKE, v_scale_ptr=FAKE)   # scales are required
+    n = _plan(k_len, batch * kv_heads, int8)
+    rows = batch * heads
+    assert attn.attn_decode_workspace_size(base_problem(**kw)) == _r256(rows * n * D * 4) + _r256(rows * n * 4)
+
+
 def test_combine_checks(L):
     assert attn.attn_combine(4, 0, 64, None, None, 0, None, 64, None, 0, None) == 0
     assert attn.attn_combine(4, 3, 0, FAKE, FAKE, 0, FAKE, 64, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
