@@ -24,10 +24,11 @@ ATTN_CAUSAL_FIXED, ATTN_CAUSAL_KLENS = 0, 1
 ATTN_KLENS_COUNT, ATTN_KLENS_LAST_INDEX = 0, 1
 ATTN_KV_AS_Q, ATTN_KV_INT8 = 0, 1
 ATTN_KV_SCALE_TENSOR, ATTN_KV_SCALE_CHANNEL = 0, 1
+ATTN_INJECT_NONE, ATTN_INJECT_DROP_FIRST_COPY = 0, 1
 DTYPE_CODE = {"f32": ATTN_F32, "f16": ATTN_F16, "bf16": ATTN_BF16}
 EXPORTS = ("attn_fwd_workspace_size", "attn_fwd", "attn_decode_workspace_size", "attn_decode", "attn_combine",
            "attn_device_status", "attn_status_string", "attn_version", "attn_decode_noalloc",
-           "attn_decode_noalloc_max_scratch", "attn_decode_append", "attn_probe_ex2")
+           "attn_decode_noalloc_max_scratch", "attn_decode_append", "attn_probe_ex2", "attn_test_inject")
 
 
 class attn_layout(ctypes.Structure):
@@ -86,6 +87,7 @@ def lib():
         L.attn_decode_append.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.attn_decode_append.restype = ctypes.c_int
         L.attn_probe_ex2.argtypes, L.attn_probe_ex2.restype = [i32, i32, vp, vp], ctypes.c_int
+        L.attn_test_inject.argtypes, L.attn_test_inject.restype = [i32], ctypes.c_int
         _lib = L
     return _lib
 
@@ -125,6 +127,11 @@ def attn_decode_append(p, q, k_new, v_new, k_cache, v_cache, o, mask, k_lens, ls
 def attn_probe_ex2(blocks, iters, sink, stream) -> int:
     """Launch the exponential-throughput micro-kernel (a measurement utility; see include/attn.h)."""
     return lib().attn_probe_ex2(blocks, iters, sink, stream)
+
+
+def attn_test_inject(fault: int) -> int:
+    """Arm the one-shot bounded-wait test fault (a test utility; see include/attn.h)."""
+    return lib().attn_test_inject(fault)
 
 
 def attn_decode_noalloc_max_scratch() -> int:

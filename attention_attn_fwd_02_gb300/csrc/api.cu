@@ -9,6 +9,10 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "prefill_tc.h"
 #include "decode.h"
@@ -19,20 +23,86 @@ namespace attn {
 // ATTN_ERR_DEVICE_TIMEOUT here; attn_device_status reads and clears it.
 __device__ int g_status_word;
 
+// One-shot fault for the bounded-wait tests (attn_test_inject): the next
+// launch of a kernel that supports it takes it and clears it.
+std::atomic<int> g_inject{ATTN_INJECT_NONE};
+
+int take_injection() { return g_inject.exchange(ATTN_INJECT_NONE); }
+
 namespace {
 
-constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices];
+using PFN_ctx_current = CUresult (*)(CUcontext*);
+using PFN_ctx_id = CUresult (*)(CUcontext, unsigned long long*);
+
+// Driver entry points for the current context and its process-unique id,
+// reached through the runtime (no libcuda link).  Null when unavailable.
+void ctx_fns(PFN_ctx_current* cur, PFN_ctx_id* id) {
+  static PFN_ctx_current f_cur = nullptr;
+  static PFN_ctx_id f_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f_cur = reinterpret_cast<PFN_ctx_current>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f_id = reinterpret_cast<PFN_ctx_id>(p);
+  });
+  *cur = f_cur;
+  *id = f_id;
+}
+
+// Id of the calling thread's current context; 0 when there is none yet or
+// the driver cannot say.
+unsigned long long current_ctx_id() {
+  PFN_ctx_current cur;
+  PFN_ctx_id id;
+  ctx_fns(&cur, &id);
+  CUcontext c = nullptr;
+  unsigned long long v = 0;
+  if (!cur || !id || cur(&c) != CUDA_SUCCESS || !c || id(c, &v) != CUDA_SUCCESS) return 0;
+  return v;
+}
+
+}  // namespace
+
+int symbol_address(SymbolCache& cache, const void* symbol, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(cache.mu);
+  unsigned long long ctx = current_ctx_id();
+  for (int i = 0; i < cache.n; ++i)
+    if (cache.dev[i] == dev && cache.ctx[i] == ctx && ctx != 0) {
+      *out = cache.ptr[i];
+      return ATTN_OK;
+    }
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, symbol) != cudaSuccess || !ptr) return ATTN_ERR_CUDA;
+  if (ctx == 0) ctx = current_ctx_id();   // the lookup above made the device's context current
+  int slot = -1;
+  for (int i = 0; i < cache.n; ++i)
+    if (cache.dev[i] == dev) slot = i;    // a context of this device seen before: replace it
+  if (slot < 0 && cache.n < SymbolCache::kSlots) slot = cache.n++;
+  if (slot >= 0) {
+    cache.dev[slot] = dev;
+    cache.ctx[slot] = ctx;
+    cache.ptr[slot] = ptr;
+  }
+  *out = ptr;
+  return ATTN_OK;
+}
+
+namespace {
+
+SymbolCache g_status_cache;
 
 int status_ptr(int** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  if (!g_status_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
-    g_status_ptr[dev] = static_cast<int*>(ptr);
-  }
-  *out = g_status_ptr[dev];
+  void* ptr = nullptr;
+  const int rc = symbol_address(g_status_cache, (const void*)&g_status_word, &ptr);
+  if (rc) return rc;
+  *out = static_cast<int*>(ptr);
   return ATTN_OK;
 }
 
@@ -327,6 +397,12 @@ int attn_probe_ex2(int32_t blocks, int32_t iters, float* sink, attn_stream strea
   return from_cuda(launch_ex2_probe(blocks, iters, sink, static_cast<cudaStream_t>(stream)));
 }
 
-int attn_version(void) { return 230; }
+int attn_test_inject(int32_t fault) {
+  if (fault != ATTN_INJECT_NONE && fault != ATTN_INJECT_DROP_FIRST_COPY) return ATTN_ERR_INVALID_ARG;
+  attn::g_inject.store(fault);
+  return ATTN_OK;
+}
+
+int attn_version(void) { return 240; }
 
 }  // extern "C"

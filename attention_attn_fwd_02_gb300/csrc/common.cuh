@@ -193,6 +193,28 @@ inline cudaError_t ensure_smem(const void* kern, int bytes) {
   return e;
 }
 
+// Device addresses of a __device__ symbol, per (device, context).  A host
+// program's name for a __device__ variable is a host-side stand-in, so the
+// address kernels need is looked up with cudaGetSymbolAddress once for each
+// device and context: after a cudaDeviceReset the device gets a new context
+// whose copy of the symbol may sit elsewhere, and the id changes with it.
+struct SymbolCache {
+  static constexpr int kSlots = 64;
+  std::mutex mu;
+  int dev[kSlots];
+  unsigned long long ctx[kSlots];
+  void* ptr[kSlots];
+  int n = 0;
+};
+// Address of `symbol` (the host stand-in's address) on the current device;
+// returns an ATTN_* status.
+int symbol_address(SymbolCache& cache, const void* symbol, void** out);
+
+// Takes (and clears) the one-shot test fault armed by attn_test_inject;
+// ATTN_INJECT_NONE when none is armed.  Host side, called right before a
+// launch of a kernel that supports the fault.
+int take_injection();
+
 // Host-side launchers (defined in the kernel translation units).
 cudaError_t launch_simt(const Problem& p, const Split& s, cudaStream_t st);
 cudaError_t launch_combine(const Problem& p, const Split& s, int32_t out_dtype, cudaStream_t st);

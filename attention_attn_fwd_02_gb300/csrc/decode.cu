@@ -28,12 +28,11 @@
 // in warp order at the end.  All sums have a fixed order.  Waits are bounded
 // (status word on timeout).
 //
-// Test hook: with the environment variable ATTN_TEST_DROP_FIRST_COPY=1 the
-// first CTA announces but never issues its first stage copy, so its waits run
-// out; the kernel then records ATTN_ERR_DEVICE_TIMEOUT, drains its other
-// copies and exits (a test reads the status word).  Nothing else changes.
+// Test hook: with the one-shot fault of attn_test_inject armed, the first CTA
+// announces but never issues its first stage copy, so its waits run out; the
+// kernel then records ATTN_ERR_DEVICE_TIMEOUT, drains its other copies and
+// exits (a test reads the status word).  Nothing else changes.
 #include <limits.h>
-#include <stdlib.h>
 
 #include <type_traits>
 
@@ -444,8 +443,8 @@ int launch_mma(const Problem& p, const Split& s, cudaStream_t st) {
   auto kern = decode_mma_kernel<BF16>;
   if (ensure_smem((const void*)kern, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  const char* drop = getenv("ATTN_TEST_DROP_FIRST_COPY");
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mk, mv, p, s, n_hc, drop && drop[0] == '1' ? 1 : 0);
+  const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mk, mv, p, s, n_hc, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

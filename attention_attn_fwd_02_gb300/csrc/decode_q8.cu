@@ -108,7 +108,8 @@ __device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
 template <bool BF16, int NT>
 __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v,
-                                                             const Problem p, const Split sp, const int n_hc) {
+                                                             const Problem p, const Split sp, const int n_hc,
+                                                             const int drop_first_copy) {
   constexpr int kHc = 8 * NT;   // query heads per CTA (MMA columns)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
     const int row0 = (int)(start + (int64_t)ch * kStageKeys);
     uint8_t* ks = smem + s * 2 * kTile;
     mbar_expect_tx(&full[s], 2 * kTile);
+    if (drop_first_copy && ch == 0 && blockIdx.x == 0) return;  // test hook: the stage never lands
     tma_load_4d(ks, &tm_k, &full[s], 0, row0, g, b);
     tma_load_4d(ks + kTile, &tm_v, &full[s], 0, row0, g, b);
   };
@@ -417,7 +419,8 @@ int launch(const Problem& p, const Split& s, cudaStream_t st) {
   const int smem = kStages * 2 * kTile + 1024;
   auto kern = decode_q8_kernel<BF16, NT>;
   if (ensure_smem((const void*)kern, smem) != cudaSuccess) return ATTN_ERR_CUDA;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mk, mv, p, s, n_hc);
+  const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mk, mv, p, s, n_hc, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -13,7 +13,8 @@
 // on which this library is loaded holds until the process exits.  Its device
 // address is looked up once per device (cudaGetSymbolAddress with that device
 // current) on the first call made on that device: make that first call before
-// any stream capture begins.  In host code the array's name stands for a host
+// any stream capture begins.  The address is kept per CUDA context, so a call
+// after a cudaDeviceReset looks it up again in the device's new context.  In host code the array's name stands for a host
 // shadow, not a device address, so only the looked-up pointer is ever passed
 // to kernels.
 //
@@ -22,33 +23,21 @@
 // key range writes its empty marker), so nothing has to start at zero.  Calls
 // whose GPU work overlaps (different streams, or different host threads) race
 // on the array; serialise them, e.g. by issuing them on one stream.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace attn {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_dev[kMaxDevices];
+SymbolCache g_scratch_cache;
 
-// Device address of the array on the current device (set up once per device).
+// Device address of the array on the current device and context (looked up
+// once per device; again only if the device's context changed).
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_dev[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return ATTN_ERR_CUDA;
-    g_scratch_dev[dev] = ptr;
-  }
-  *out = g_scratch_dev[dev];
-  return ATTN_OK;
+  return symbol_address(g_scratch_cache, (const void*)&g_noalloc_scratch, out);
 }
 
 }  // namespace

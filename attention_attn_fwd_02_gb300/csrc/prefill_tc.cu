@@ -85,7 +85,7 @@ template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
-                      const int mask_bcast) {
+                      const int mask_bcast, const int drop_first_copy) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -200,7 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int krow = (j0 + i) * BN;
         if (!wait_bar(&sb.k_empty[s], ph ^ 1u, &sb.abort, p.status)) break;
         mbar_expect_tx(&sb.k_full[s], C::kKTile);
-        for (int c = 0; c < C::kChunks; ++c)
+        // Test hook (attn_test_inject): the first CTA's first K copy is
+        // announced but never issued, so the MMA warp's wait runs out.
+        const bool dropped = drop_first_copy && i == 0 && blockIdx.x == 0;
+        for (int c = 0; c < C::kChunks && !dropped; ++c)
           tma_load_4d(k_s + s * C::kKTile + c * BN * 128, &tm_k, &sb.k_full[s], c * 64, krow, g, b);
         if (!wait_bar(&sb.v_empty[s], ph ^ 1u, &sb.abort, p.status)) {
           k_only = i;
@@ -229,6 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     // ---------------- MMA issuer ----------------
+    // The whole warp runs this loop (warp-uniform control flow); one elected
+    // lane issues each tcgen05 instruction.  Each barrier the issuer needs is
+    // first tested without blocking a batch of MMAs ahead of its use, so a
+    // phase that has already completed costs no barrier round trip there.
     constexpr uint32_t kIdQK = idesc_f16(BF16, false, BM, BN);
     constexpr uint32_t kIdPV = idesc_f16(BF16, true, BM, D);
     const uint32_t q_addr = su32(q_s), k_addr = su32(k_s), v_addr = su32(v_s);
@@ -245,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t a = sdesc_add(ad, (uint32_t)((kk / 4) * BM * 128 + (kk % 4) * 32));
         const uint64_t bd = sdesc_add(bd0, (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32));
-        mma_ss(tmem + (tt ? C::kS1 : C::kS0), a, bd, kIdQK, kk > 0);
+        mma_ss_w(tmem + (tt ? C::kS1 : C::kS0), a, bd, kIdQK, kk > 0);
       }
     };
     auto issue_pv = [&](int tt, int s, bool first) {
@@ -254,25 +261,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
         const uint64_t bd = sdesc_add(bd0, (uint32_t)(kk * 16 * 128));
-        mma_ts(tmem + (tt ? C::kO1 : C::kO0), tmem + (tt ? C::kS1 : C::kS0) + kk * 8, bd, kIdPV,
-               (!first || kk > 0) ? 1u : 0u);
+        mma_ts_w(tmem + (tt ? C::kO1 : C::kO0), tmem + (tt ? C::kS1 : C::kS0) + kk * 8, bd, kIdPV,
+                 (!first || kk > 0) ? 1u : 0u);
       }
     };
     // Prologue: S0 and S1 of tile 0.
     if (ok) ok = wait_warp(&sb.k_full[0], 0, &sb.abort, p.status);
-    if (ok && lane == 0) {
+    if (ok) {
       issue_qk(0, 0);
-      mma_commit(&sb.s_full[0]);
+      mma_commit_w(&sb.s_full[0]);
       issue_qk(1, 0);
-      mma_commit(&sb.s_full[1]);
-      mma_commit(&sb.k_empty[0]);
+      mma_commit_w(&sb.s_full[1]);
+      mma_commit_w(&sb.k_empty[0]);
     }
-    __syncwarp();
+    bool rv = ok && mbar_test(&sb.v_full[0], 0);   // V(0) landed?
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int s = i % C::kStages;
       const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
       const int k0 = (j0 + i) * BN;
-      if (!wait_warp(&sb.v_full[s], ph, &sb.abort, p.status)) break;
+      const bool more = i + 1 < n_tiles;
+      const int s1 = (i + 1) % C::kStages;
+      const uint32_t ph1 = (uint32_t)((i + 1) / C::kStages) & 1u;
+      bool rp0 = mbar_test(&sb.p_full[0], (uint32_t)i & 1u);
+      if (!(ok = wait_ready(rv, &sb.v_full[s], ph, &sb.abort, p.status))) break;
       // Zero the V rows of keys no row of this CTA sees (they may hold anything).
       if (k0 < lo_u || k0 + BN > hi_u) {
         for (int u = lane; u < BN * C::kChunks * 8; u += 32) {
@@ -286,44 +297,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
       }
-      __syncwarp();
-      const bool more = i + 1 < n_tiles;
-      const int s1 = (i + 1) % C::kStages;
-      const uint32_t ph1 = (uint32_t)((i + 1) / C::kStages) & 1u;
+      const bool rk = !more || mbar_test(&sb.k_full[s1], ph1);
       // Query tile 0: P0 V, then the next S0.
-      if (!wait_warp(&sb.p_full[0], (uint32_t)i & 1u, &sb.abort, p.status)) break;
-      if (lane == 0) {
-        issue_pv(0, s, i == 0);
-        mma_commit(&sb.o_done[0]);
-      }
-      __syncwarp();
+      if (!(ok = wait_ready(rp0, &sb.p_full[0], (uint32_t)i & 1u, &sb.abort, p.status))) break;
+      issue_pv(0, s, i == 0);
+      mma_commit_w(&sb.o_done[0]);
+      const bool rp1 = mbar_test(&sb.p_full[1], (uint32_t)i & 1u);
       if (more) {
-        if (!wait_warp(&sb.k_full[s1], ph1, &sb.abort, p.status)) break;
-        if (lane == 0) {
-          issue_qk(0, s1);
-          mma_commit(&sb.s_full[0]);
-        }
+        if (!(ok = wait_ready(rk, &sb.k_full[s1], ph1, &sb.abort, p.status))) break;
+        issue_qk(0, s1);
+        mma_commit_w(&sb.s_full[0]);
       }
-      __syncwarp();
+      rv = more && mbar_test(&sb.v_full[s1], ph1);   // for the next tile
       // Query tile 1: P1 V, then the next S1.
-      if (!wait_warp(&sb.p_full[1], (uint32_t)i & 1u, &sb.abort, p.status)) break;
-      if (lane == 0) {
-        issue_pv(1, s, i == 0);
-        mma_commit(&sb.o_done[1]);
-        mma_commit(&sb.v_empty[s]);
-        if (more) {
-          issue_qk(1, s1);
-          mma_commit(&sb.s_full[1]);
-          mma_commit(&sb.k_empty[s1]);
-        }
+      if (!(ok = wait_ready(rp1, &sb.p_full[1], (uint32_t)i & 1u, &sb.abort, p.status))) break;
+      issue_pv(1, s, i == 0);
+      mma_commit_w(&sb.o_done[1]);
+      mma_commit_w(&sb.v_empty[s]);
+      if (more) {
+        issue_qk(1, s1);
+        mma_commit_w(&sb.s_full[1]);
+        mma_commit_w(&sb.k_empty[s1]);
       }
-      __syncwarp();
     }
     // Every MMA issued above has completed before TMEM is freed.
-    if (lane == 0 && n_tiles > 0) {
-      mma_commit(&sb.mma_done);
-      drain_bar(&sb.mma_done, 0, p.status);
+    if (n_tiles > 0) {
+      mma_commit_w(&sb.mma_done);
+      if (lane == 0) drain_bar(&sb.mma_done, 0, p.status);
     }
     __syncwarp();
   } else if (warp >= 10) {
@@ -602,7 +604,8 @@ int launch(const Problem& p, cudaStream_t st) {
                           (reinterpret_cast<uintptr_t>(p.M) & 15) == 0 && p.Sk % 4 == 0)
                              ? 1
                              : 0;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, mask_bcast);
+  const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, mask_bcast, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

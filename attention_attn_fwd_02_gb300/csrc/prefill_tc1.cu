@@ -126,7 +126,8 @@ struct UnitSeq {
 template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks) {
+                       const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
+                       const int drop_first_copy) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -213,7 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&sb.full[u], kUnit);
         uint8_t* dst = ring + u * kUnit;
         const int krow = (j0 + tile) * BN;
-        if (kind == 0) {
+        if (drop_first_copy && issued == 0 && blockIdx.x == 0) {
+          // Test hook (attn_test_inject): the first CTA's first unit is
+          // announced but never copied, so the MMA warp's wait runs out.
+        } else if (kind == 0) {
           // head-dim half `half` of K rows [krow, krow + 128): two 64-column chunks
           for (int c = 0; c < 2; ++c)
             tma_load_4d(dst + c * BN * 128, &tm_k, &sb.full[u], (2 * half + c) * 64, krow, g, b);
@@ -232,48 +236,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
+    // The whole warp runs this code (warp-uniform control flow); one elected
+    // lane issues each tcgen05 instruction.  The next ring unit's barrier and
+    // the next P's barrier are tested without blocking a batch of MMAs ahead
+    // of their use, so a phase that has already completed costs no barrier
+    // round trip where the unit or P is taken.
     constexpr uint32_t kIdQK = idesc_f16(BF16, false, BM, BN);
     constexpr uint32_t kIdPV = idesc_f16(BF16, true, BM, D);
     const uint32_t q_addr = su32(q_s), ring_addr = su32(ring);
     // Descriptors of the operand tiles' starts; the K-steps add constants.
     const uint64_t qd = sdesc(q_addr, 16, 1024), ud = sdesc(ring_addr, 16, 1024),
                    vd = sdesc(ring_addr, (BN / 2) * 128, 1024);
-    int taken = 0;  // units consumed so far (ring position)
+    int taken = 0;        // units consumed so far (ring position)
+    bool next_ready = false;   // early test of unit `taken`
     bool ok = n_tiles > 0;
-    // Waits for the next unit; returns its shared address (0 on abort).
+    // Waits for the next unit; returns its shared address (0 on abort), and
+    // tests the unit after it.
     auto take = [&]() -> uint32_t {
       const int u = taken % kUnits;
       const uint32_t ph = (uint32_t)(taken / kUnits) & 1u;
       ++taken;
-      if (!wait_warp(&sb.full[u], ph, &sb.abort, p.status)) return 0u;
+      if (!wait_ready(next_ready, &sb.full[u], ph, &sb.abort, p.status)) return 0u;
+      next_ready = mbar_test(&sb.full[taken % kUnits], (uint32_t)(taken / kUnits) & 1u);
       return ring_addr + (uint32_t)(u * kUnit);
     };
     // The unit just taken is released when the MMAs issued so far complete.
-    auto give = [&]() {
-      if (lane == 0) mma_commit(&sb.empty[(taken - 1) % kUnits]);
-    };
+    auto give = [&]() { mma_commit_w(&sb.empty[(taken - 1) % kUnits]); };
     // S[slot] = Q K(tile)^T: 16 MMAs of K = 16, the first 8 from the low
     // head-dim half of K, the rest from the high half.
     auto issue_qk = [&](int slot) -> bool {
       for (int hf = 0; hf < 2; ++hf) {
         const uint32_t ku = take();
         if (!ku) return false;
-        if (lane == 0) {
-          fence_after();
-          const uint64_t bd0 = sdesc_add(ud, ku - ring_addr);
+        fence_after();
+        const uint64_t bd0 = sdesc_add(ud, ku - ring_addr);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int kq = hf * 8 + kk;  // K-step over head_dim
-            const uint64_t a = sdesc_add(qd, (uint32_t)((kq / 4) * BM * 128 + (kq % 4) * 32));
-            const uint64_t bd = sdesc_add(bd0, (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32));
-            mma_ss(tmem + (slot ? C::kS1 : C::kS0), a, bd, kIdQK, kq > 0);
-          }
+        for (int kk = 0; kk < 8; ++kk) {
+          const int kq = hf * 8 + kk;  // K-step over head_dim
+          const uint64_t a = sdesc_add(qd, (uint32_t)((kq / 4) * BM * 128 + (kq % 4) * 32));
+          const uint64_t bd = sdesc_add(bd0, (uint32_t)((kk / 4) * BN * 128 + (kk % 4) * 32));
+          mma_ss_w(tmem + (slot ? C::kS1 : C::kS0), a, bd, kIdQK, kq > 0);
         }
-        __syncwarp();
         give();
       }
-      if (lane == 0) mma_commit(&sb.s_full[slot]);
-      __syncwarp();
+      mma_commit_w(&sb.s_full[slot]);
       return true;
     };
     // O += P[slot] V(tile): 8 MMAs of K = 16 keys, 4 per V unit.
@@ -294,40 +300,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                   make_uint4(0, 0, 0, 0);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
         }
-        __syncwarp();
-        if (lane == 0) {
-          fence_after();
-          const uint64_t bd0 = sdesc_add(vd, vu - ring_addr);
+        fence_after();
+        const uint64_t bd0 = sdesc_add(vd, vu - ring_addr);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_add(bd0, (uint32_t)(kk * 16 * 128));
-            mma_ts(tmem + C::kO, tmem + (slot ? C::kS1 : C::kS0) + (hf * 4 + kk) * 8, bd, kIdPV,
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = sdesc_add(bd0, (uint32_t)(kk * 16 * 128));
+          mma_ts_w(tmem + C::kO, tmem + (slot ? C::kS1 : C::kS0) + (hf * 4 + kk) * 8, bd, kIdPV,
                    (!first || hf > 0 || kk > 0) ? 1u : 0u);
-          }
         }
-        __syncwarp();
         give();
       }
-      if (lane == 0) mma_commit(&sb.o_done);
-      __syncwarp();
+      mma_commit_w(&sb.o_done);
       return true;
     };
     if (ok) ok = wait_warp(&sb.q_full, 0, &sb.abort, p.status);
     // Prologue: S of the first two key tiles.
     for (int j = 0; ok && j < 2 && j < n_tiles; ++j) ok = issue_qk(j);
+    bool rp = ok && mbar_test(&sb.p_full[0], 0u);
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int slot = i & 1;
-      if (!(ok = wait_warp(&sb.p_full[slot], (uint32_t)(i >> 1) & 1u, &sb.abort, p.status))) break;
+      if (!(ok = wait_ready(rp, &sb.p_full[slot], (uint32_t)(i >> 1) & 1u, &sb.abort, p.status))) break;
       if (!(ok = issue_pv(slot, i, i == 0))) break;
+      if (i + 1 < n_tiles) rp = mbar_test(&sb.p_full[slot ^ 1], (uint32_t)((i + 1) >> 1) & 1u);
       // Q K^T of tile i+2 into the S buffer P(i) just left (the tensor core
       // runs a thread's MMAs in issue order, so P V(i) reads P first).
       if (i + 2 < n_tiles && !(ok = issue_qk(slot))) break;
     }
     // Every MMA issued above has completed before TMEM is freed.
-    if (lane == 0 && taken > 0) {
-      mma_commit(&sb.mma_done);
-      drain_bar(&sb.mma_done, 0, p.status);
+    if (taken > 0) {
+      mma_commit_w(&sb.mma_done);
+      if (lane == 0) drain_bar(&sb.mma_done, 0, p.status);
     }
     __syncwarp();
   } else {
@@ -565,7 +569,8 @@ int launch(const Problem& p, cudaStream_t st) {
   auto kern = prefill_tc1_kernel<D, BF16, MASK>;
   cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb);
+  const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -45,6 +45,21 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with parity `parity` (acquire on success).
+// Its result returns after the shared-memory round trip (~200 cycles), so a
+// test issued a batch of MMAs ahead of its use costs no wait at the use.
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of `b` with parity `parity`.
 __device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, int* abort_flag, int* status) {
   if (mbar_try(b, parity)) return true;
@@ -78,6 +93,13 @@ __device__ __forceinline__ bool drain_bar(uint64_t* b, uint32_t parity, int* sta
 __device__ __forceinline__ bool wait_warp(uint64_t* b, uint32_t parity, int* abort_flag, int* status) {
   const bool ok = wait_bar(b, parity, abort_flag, status);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-uniform bounded wait that skips the barrier round trip when an earlier
+// non-blocking test (`ready`) already saw the phase complete in every lane.
+__device__ __forceinline__ bool wait_ready(bool ready, uint64_t* b, uint32_t parity, int* abort_flag, int* status) {
+  if (__all_sync(0xffffffffu, ready)) return true;
+  return wait_warp(b, parity, abort_flag, status);
 }
 
 // Contiguous bulk copy global -> shared, completing on `bar` (both addresses
@@ -120,6 +142,37 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// Warp-wide forms: every lane of a converged warp executes the statement and
+// elect.sync picks the one lane that issues.  The operands are warp-uniform,
+// and the issuing thread is not a divergent branch of its warp; measured on
+// GB300 this issues a tcgen05.mma in ~35-44 cycles against ~48-54 for the
+// same instruction under `if (lane == 0)`.
+__device__ __forceinline__ void mma_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t* b) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(b))
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
                : "memory");

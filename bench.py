@@ -53,6 +53,25 @@ def peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+    except (OSError, subprocess.SubprocessError):
+        out = ""
+    for line in out.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -255,7 +274,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(walls)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": case.name, "sample": f"{rows} random query rows over {args.steps} steps"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": f"{rows} random query rows of {case.name}, float64 three-pass oracle"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -449,8 +468,23 @@ def run_ours(args):
         e_end.record(s_out)
         torch.cuda.synchronize()
         (e_s,) = max_over_ranks([e_start.elapsed_time(e_end) / 1e3], world, dev)
+        # The host link's own rates on the same pinned buffers (best of three
+        # single copies of Q in and O out), to read the e2e number against.
+        def copy_gbs(dst, src):
+            best = 0.0
+            for _ in range(3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                dst.copy_(src, non_blocking=True)
+                b.record(stream)
+                b.synchronize()
+                best = max(best, src.numel() * src.element_size() / (a.elapsed_time(b) / 1e3) / 1e9)
+            return best
+        h2d_gbs, d2h_gbs = copy_gbs(bufs[0][0], hq), copy_gbs(ho[0], bufs[0][4])
         e2e = {"value": job_throughput(flops, world, steps, e_s) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+               "copy_bound_tflops": flops / (h2d / (h2d_gbs * 1e9)) / 1e12,
                "pipelining": "copies in, compute and copies out on three streams, two buffer sets"}
 
     pk, pk_kind = peaks()
@@ -458,6 +492,9 @@ def run_ours(args):
     pre_launch_s = pre_s / steps
     roof = {"bound": "tensor", "achieved": flops / pre_launch_s / 1e12, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s", "frac": flops / pre_launch_s / 1e12 / pk["bf16_tflops"],
+            "peak_sustained": pk.get("bf16_tflops_sustained"),
+            "frac_sustained": (flops / pre_launch_s / 1e12 / pk["bf16_tflops_sustained"]
+                               if pk.get("bf16_tflops_sustained") else None),
             "traffic": ncu_traffic("prefill_tc", digest), "kernel": "attn::tc::prefill_tc_kernel<128,bf16>",
             "peak_kind": f"{pk_kind} bf16 dense, burst", "algorithmic_flops_per_launch": flops}
     dec_roof = {"bound": "hbm", "achieved": kv_bytes / (dec_s / steps) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -481,8 +518,12 @@ def run_ours(args):
         oracle.build()
         cores = oracle.default_threads()
         cv, n, dt = oracle_prefill_sample(pf, 10.0, cores)
-        cpu = {"value": cv, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} random query rows of {pf.name} ({dt:.1f} s wall)"}
+        cpu = {"value": cv, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+               "sample": f"{n} random query rows of {pf.name} ({dt:.1f} s wall)",
+               "single_thread": oracle_single_thread()}
+    cases = None
+    if rank == 0 and world == 1 and not args.no_cases and args.only is None:
+        cases = extra_cases(pk, pk_kind)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s / steps, "higher_is_better": True, "scaling": "weak",
@@ -497,6 +538,9 @@ def run_ours(args):
         "prefill_ms_per_step": 1e3 * pre_s / steps,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "extra": {"cases": cases,
+                  "note": "per-call device times of the other workloads (median, L2 flushed before each call), "
+                          "measured after the timed region; not part of value"},
         "gpu_launches": steps * ((args.only != "decode") + 2 * (args.only != "prefill")),
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
@@ -522,6 +566,47 @@ CASES = {
 }
 
 
+def time_case(case, steps: int, warmup: int, flush: bool = True):
+    """Median and minimum device time (ms) of one call of `case` through the C ABI,
+    inputs resident in HBM, an L2 flush (256 MiB write) before each timed call."""
+    import torch
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import GpuCase
+    g = GpuCase(case, lse=True, guard=0)
+    fl = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush else None
+    for _ in range(warmup):
+        g.run()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ms = []
+    for _ in range(steps):
+        if fl is not None:
+            fl.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g.run()
+        e1.record(st)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return statistics.median(ms), min(ms)
+
+
+def case_line(case, med_ms: float, pk: dict, pk_kind: str) -> dict:
+    """Throughput of one call: decode KV GB/s against the HBM copy peak, prefill TFLOP/s
+    against the bf16 peaks (burst and sustained)."""
+    p = case.problem
+    if case.decode:
+        by = decode_kv_bytes(case)
+        v = by / (med_ms / 1e3) / 1e9
+        return {"unit": "GB/s", "value": v, "algorithmic_bytes": by, "frac": v / pk["hbm_gbs"],
+                "peak_kind": f"{pk_kind} HBM copy"}
+    fl = 4.0 * p["head_dim"] * wl.visible_pairs(case)
+    v = fl / (med_ms / 1e3) / 1e12
+    return {"unit": "TFLOP/s", "value": v, "algorithmic_flops": fl, "frac": v / pk["bf16_tflops"],
+            "frac_sustained": v / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+            "peak_kind": f"{pk_kind} bf16 dense (burst; sustained beside it)"}
+
+
 def run_case(args):
     """Time one call of one named workload (inputs resident in HBM) and print a per-case line.
 
@@ -530,44 +615,56 @@ def run_case(args):
     unless --no-flush is given; the line reports the median call time."""
     import torch
     from attention_attn_fwd_02_gb300 import attn, build
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_util import GpuCase
     build.build()
     attn.lib()
     torch.cuda.set_device(0)
     case = CASES[args.case]()
-    p = case.problem
-    g = GpuCase(case, lse=True, guard=0)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    for _ in range(args.warmup):
-        g.run()
-    torch.cuda.synchronize()
-    st = torch.cuda.current_stream()
-    ms = []
-    for _ in range(args.steps):
-        if not args.no_flush:
-            flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        g.run()
-        e1.record(st)
-        e1.synchronize()
-        ms.append(e0.elapsed_time(e1))
+    med, mn = time_case(case, args.steps, args.warmup, flush=not args.no_flush)
     rc = attn.attn_device_status()
-    med = statistics.median(ms)
     pk, pk_kind = peaks()
     line = {"line": "case", "case": case.name, "steps": args.steps, "warmup": args.warmup, "ms_median": med,
-            "ms_min": min(ms), "l2": "not flushed" if args.no_flush else "flushed (256 MiB write) before each call",
+            "ms_min": mn, "l2": "not flushed" if args.no_flush else "flushed (256 MiB write) before each call",
             "status": attn.status_string(rc)}
-    if case.decode:
-        by = decode_kv_bytes(case)
-        line.update({"unit": "GB/s", "value": by / (med / 1e3) / 1e9, "algorithmic_bytes": by,
-                     "frac": by / (med / 1e3) / 1e9 / pk["hbm_gbs"], "peak_kind": f"{pk_kind} HBM copy"})
-    else:
-        fl = 4.0 * p["head_dim"] * wl.visible_pairs(case)
-        line.update({"unit": "TFLOP/s", "value": fl / (med / 1e3) / 1e12, "algorithmic_flops": fl,
-                     "frac": fl / (med / 1e3) / 1e12 / pk["bf16_tflops"], "peak_kind": f"{pk_kind} bf16 dense, burst"})
+    line.update(case_line(case, med, pk, pk_kind))
     print(json.dumps(line), flush=True)
+
+
+# Workloads timed per call inside the default benchmark run (after its timed
+# region) so their numbers sit in the same record: the tiny float32 MHA, the
+# causal GQA with documents, the head_dim-256 masked cross-attention in both
+# MaskedRows modes, and the context cases.
+EXTRA_CASES = ("tiny_f32_mha", "gqa_doc_causal_bf16", "cross_mask_f16", "cross_mask_f16_zero", "dense_gqa_bf16",
+               "masked_gqa_bf16", "decode_bnsh_int8")
+
+
+def extra_cases(pk, pk_kind):
+    from attention_attn_fwd_02_gb300 import attn
+    out = {}
+    for name in EXTRA_CASES:
+        case = CASES[name]()
+        small = name in ("tiny_f32_mha", "gqa_doc_causal_bf16")
+        med, mn = time_case(case, 50 if small else 10, 5 if small else 3)
+        d = {"workload": case.name, "ms_median": med, "ms_min": mn}
+        d.update(case_line(case, med, pk, pk_kind))
+        d["status"] = attn.status_string(attn.attn_device_status())
+        out[name] = d
+    return out
+
+
+def oracle_single_thread(names=("tiny_f32_mha", "gqa_doc_causal_bf16")):
+    """Wall time of the float64 oracle on ONE host thread over the whole of the small workloads."""
+    import oracle
+    oracle.build()
+    out = {}
+    for name in names:
+        case = CASES[name]()
+        p = case.problem
+        t0 = time.perf_counter()
+        oracle.attn(p, case.q, case.k, case.v, mask=case.mask, seg=case.seg, k_lens=case.k_lens, nthreads=1)
+        dt = time.perf_counter() - t0
+        fl = 4.0 * p["head_dim"] * wl.visible_pairs(case)
+        out[name] = {"workload": case.name, "seconds": dt, "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": 1}
+    return out
 
 
 def main():
@@ -579,6 +676,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--no-cases", action="store_true", help="skip the per-call lines of the other workloads")
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="batch of the decode workload (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,

@@ -269,6 +269,21 @@ ATTN_API const char* attn_status_string(int status);
  * launch fails. */
 ATTN_API int attn_probe_ex2(int32_t blocks, int32_t iters, float* sink, attn_stream stream);
 
+/* Test utility, not part of the attention path: arms a one-shot fault for the
+ * tests of the kernels' bounded waits.  With ATTN_INJECT_DROP_FIRST_COPY, the
+ * next launch of a tensor-core kernel (the prefill kernels and the decode
+ * split passes; the CUDA-core kernels ignore it and leave it armed) makes its
+ * first CTA announce its first key-tile copy to the copy's barrier without
+ * issuing it.  The waits on that barrier then run out after about 2 s; the CTA
+ * records ATTN_ERR_DEVICE_TIMEOUT in the status word (attn_device_status),
+ * waits (bounded) for the copies and tensor-core work it did start, frees its
+ * tensor memory and exits, so the context stays usable.  That call's outputs
+ * are undefined; later calls are unaffected.  ATTN_INJECT_NONE disarms.
+ * The fault is process-wide and host-side: nothing outside this call arms it.
+ * Returns ATTN_ERR_INVALID_ARG for an unknown code. */
+enum { ATTN_INJECT_NONE = 0, ATTN_INJECT_DROP_FIRST_COPY = 1 };
+ATTN_API int attn_test_inject(int32_t fault);
+
 /* Library version as major*10000 + minor*100 + patch. */
 ATTN_API int attn_version(void);
 

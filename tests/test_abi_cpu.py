@@ -195,4 +195,13 @@ def test_status_strings_and_version(L):
     for code in range(7):
         assert attn.status_string(code) and attn.status_string(code) != "unknown status"
     assert attn.status_string(99) == "unknown status"
-    assert attn.attn_version() >= 230
+    assert attn.attn_version() >= 240
+
+
+def test_test_inject_checks(L):
+    """The one-shot test fault: known codes are accepted (and disarmed again
+    here, so no later launch takes it); unknown codes are rejected."""
+    assert attn.attn_test_inject(attn.ATTN_INJECT_DROP_FIRST_COPY) == attn.ATTN_OK
+    assert attn.attn_test_inject(attn.ATTN_INJECT_NONE) == attn.ATTN_OK
+    assert attn.attn_test_inject(7) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_test_inject(-1) == attn.ATTN_ERR_INVALID_ARG

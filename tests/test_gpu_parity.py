@@ -84,6 +84,12 @@ EDGE = [
     ("f16", "bshd", 1, 2, 1, 127, 127, 200, False, None, False, False, "11qk", "zero", True),
     ("bf16", "bhsd", 3, 2, 2, 1, 513, 128, False, None, False, True, None, "nan", False),
     ("f32", "bhsd", 1, 2, 2, 300, 300, 256, True, None, False, False, None, "nan", False),
+    # float32 at odd head dims around the thread-per-row splits (CUDA-core path)
+    ("f32", "bshd", 2, 2, 1, 45, 70, 63, True, None, False, True, None, "nan", False),
+    ("f32", "bhsd", 1, 3, 3, 33, 100, 65, False, None, False, False, "bhqk", "nan", False),
+    ("f32", "bshd", 1, 2, 2, 40, 40, 127, True, 0, True, False, None, "zero", False),
+    ("f32", "bhsd", 2, 2, 1, 20, 77, 129, False, None, False, True, "b11k", "nan", False),
+    ("f32", "bshd", 1, 2, 1, 30, 50, 255, True, None, False, False, None, "nan", False),
     # head_dim 256 with two and three key tiles: the last P V may still be two phases behind
     ("bf16", "bhsd", 2, 4, 2, 200, 100, 256, False, None, False, False, None, "nan", False),
     ("f16", "bshd", 1, 3, 1, 260, 190, 256, True, None, False, True, None, "zero", False),
@@ -225,10 +231,10 @@ def test_key_range_split_then_combine_equals_one_call():
     assert np.max(np.abs(l.cpu().numpy().reshape(B, H, Sq) - full_l)) <= 1e-3
 
 
-def test_prefill_without_workspace_uses_static_schedule():
-    """attn_fwd accepts a null workspace (the tensor-core kernel then walks its
-    work tiles in a static order); the result matches the oracle and, bit for
-    bit, the run with a workspace (every tile is computed the same way)."""
+def test_prefill_with_a_null_workspace_matches_the_first_call():
+    """attn_fwd called again with a null workspace and size 0 (what a caller
+    passes when attn_fwd_workspace_size returns 0) gives the same bits as the
+    first call and matches the oracle."""
     c = wl.long_causal_gqa_bf16(batch=2, seq=1500, heads=8, kv_heads=2)
     g = GpuCase(c).run()
     _, l1, o1 = g.outputs()
@@ -274,20 +280,6 @@ def test_decode_variants(i):
     st, _ = run_and_compare(c, lse=lse)
     if lens == "zero_full":
         assert st["nan_rows"] == H      # batch entry 0 has no valid key
-
-
-def test_decode_bounded_wait_reports_timeout_and_context_stays_usable(monkeypatch):
-    """A stage copy that never lands makes the split pass's bounded waits run
-    out: the kernel records ATTN_ERR_DEVICE_TIMEOUT and exits; the next call on
-    the same context is correct."""
-    c = wl.decode_bnsh_bf16(seed=77, batch=2, capacity=1024, heads=8, kv_heads=2, min_len=600)
-    monkeypatch.setenv("ATTN_TEST_DROP_FIRST_COPY", "1")
-    g = GpuCase(c).run()
-    torch_mod().cuda.synchronize()
-    assert attn.attn_device_status() == attn.ATTN_ERR_DEVICE_TIMEOUT
-    monkeypatch.delenv("ATTN_TEST_DROP_FIRST_COPY")
-    assert attn.attn_device_status() == attn.ATTN_OK      # the status word was cleared
-    run_and_compare(c)
 
 
 # ---- visibility variants: sliding window, right-aligned causal bound, last-index lengths -----------

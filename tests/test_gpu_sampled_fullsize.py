@@ -46,6 +46,7 @@ FULL = {
     "cross_mask_f16_zero": lambda: wl.cross_mask_f16(masked_rows="zero"),
     "decode_bnsh_int8": lambda: wl.decode_bnsh_int8(),
     "dense_gqa_bf16": lambda: wl.dense_gqa_bf16(),
+    "masked_gqa_bf16": lambda: wl.masked_gqa_bf16(),
 }
 
 
