@@ -61,6 +61,10 @@ constexpr int kUnit = 32768;            // bytes per unit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kSlack = 8.0f;          // log2 units
+// A mask broadcast over heads and rows ([B,1,1,K]) is staged for the CTA's
+// whole key range when that range holds at most this many keys.
+constexpr int kMaskCap = 4096;
+constexpr int kMaxListTiles = kMaskCap / BN;
 
 struct Bars {
   uint64_t q_full;
@@ -71,15 +75,19 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
   int lo_u, hi_u;
+  uint32_t live;             // staged mask: bit t set when key tile j0 + t has a key of non -inf mask
+  int n_live;
+  uint8_t list[kMaxListTiles];   // staged mask: the live key tiles, relative to j0, in order
   float red_max[2][2][BM];   // [tile parity][key half][row]: partial tile maxima
   float red_l[2][BM];        // [key half][row]: partial sums for the epilogue
 };
 
-template <int D>
+template <int D, bool MASK>
 struct Cfg {
   static_assert(D == 256, "this kernel is laid out for head_dim 256");
   static constexpr int kQTile = BM * D * 2;                      // 64 KB
-  static constexpr int kSmem = kQTile + kUnits * kUnit;          // 192 KB
+  static constexpr int kMaskBytes = MASK ? kMaskCap * 4 : 0;     // staged broadcast mask (16 KB)
+  static constexpr int kSmem = kQTile + kUnits * kUnit + kMaskBytes;   // 192 or 208 KB
   static constexpr int kS0 = 0, kS1 = BN, kO = 2 * BN;
   static_assert(kO + D <= 512, "TMEM budget");
   // A K unit holds one head-dim half of a key tile: 2 chunks of [128 keys][128 B].
@@ -127,12 +135,13 @@ template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
-                       const int drop_first_copy) {
-  using C = Cfg<D>;
+                       const int drop_first_copy, const int mask_stage) {
+  using C = Cfg<D, MASK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;
   uint8_t* ring = q_s + C::kQTile;
+  float* m_s = reinterpret_cast<float*>(ring + kUnits * kUnit);   // staged mask values (MASK only)
   __shared__ Bars sb;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -155,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
     sb.lo_u = 0x7fffffff;
     sb.hi_u = -1;
+    sb.live = 0u;
+    sb.n_live = 0;
     sb.abort = 0;
     mbar_init(&sb.q_full, 1);
     for (int u = 0; u < kUnits; ++u) {
@@ -200,7 +211,76 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lo_u = sb.lo_u, hi_u = sb.hi_u;
   const bool any = hi_u > lo_u;
   const int j0 = any ? lo_u / BN : 0;
-  const int n_tiles = any ? (hi_u + BN - 1) / BN - j0 : 0;
+  const int n_span = any ? (hi_u + BN - 1) / BN - j0 : 0;   // key tiles spanning the union
+  // A broadcast mask over a span of at most kMaskCap keys is copied to shared
+  // memory once (every softmax thread reads it there), and key tiles whose
+  // visible keys all have mask -inf are dropped from the CTA's work: their
+  // probabilities are zero, so neither the maximum, the sum nor O sees them.
+  // NaN or +inf entries keep their tile (they make rows NaN).
+  const int mbase = j0 * BN;
+  const bool staged = MASK && mask_stage && n_span > 0 && n_span <= kMaxListTiles;
+  if (staged) {
+    // Every thread issues all of its loads before using any (one memory round
+    // trip), stores the values and marks the tiles of its keys that are live.
+    const int mlen = min(p.Sk, (j0 + n_span) * BN) - mbase;
+    const float* src = p.M + p.m.off + (int64_t)b * p.m.bs + mbase;
+    uint32_t mine = 0u;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      constexpr int kVec = (kMaskCap / 4 + kThreads - 1) / kThreads;
+      float4 v[kVec];
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) {
+        const int k = 4 * (threadIdx.x + j * kThreads);
+        v[j] = k + 3 < mlen ? __ldg(reinterpret_cast<const float4*>(src + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < mlen && k + 3 >= mlen) {   // the ragged end
+          v[j].x = src[k];
+          v[j].y = k + 1 < mlen ? src[k + 1] : -INFINITY;
+          v[j].z = k + 2 < mlen ? src[k + 2] : -INFINITY;
+          v[j].w = -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) {
+        const int k = 4 * (threadIdx.x + j * kThreads);
+        if (k >= mlen) continue;
+        reinterpret_cast<float4*>(m_s)[k / 4] = v[j];
+        const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int key = mbase + k + q;
+          if (k + q < mlen && key >= lo_u && key < hi_u && !(e[q] == -INFINITY)) mine |= 1u << ((k + q) / BN);
+        }
+      }
+    } else {
+      constexpr int kSc = (kMaskCap + kThreads - 1) / kThreads;
+      float v[kSc];
+#pragma unroll
+      for (int j = 0; j < kSc; ++j) {
+        const int k = threadIdx.x + j * kThreads;
+        v[j] = k < mlen ? src[k] : -INFINITY;
+      }
+#pragma unroll
+      for (int j = 0; j < kSc; ++j) {
+        const int k = threadIdx.x + j * kThreads;
+        if (k >= mlen) continue;
+        m_s[k] = v[j];
+        const int key = mbase + k;
+        if (key >= lo_u && key < hi_u && !(v[j] == -INFINITY)) mine |= 1u << (k / BN);
+      }
+    }
+    mine = __reduce_or_sync(0xffffffffu, mine);
+    if (lane == 0 && mine) atomicOr(&sb.live, mine);
+    __syncthreads();
+    // The i-th live tile is the i-th set bit of the live mask.
+    const uint32_t live = sb.live;
+    if (threadIdx.x < (unsigned)n_span && ((live >> threadIdx.x) & 1u))
+      sb.list[__popc(live & ((1u << threadIdx.x) - 1u))] = (uint8_t)threadIdx.x;
+    if (threadIdx.x == 0) sb.n_live = __popc(live);
+    __syncthreads();
+  }
+  const int n_tiles = staged ? sb.n_live : n_span;
+  // Key tile (relative to j0) of the CTA's i-th tile of work.
+  auto tile_of = [&](int i) -> int { return staged ? (int)sb.list[i] : i; };
 
   if (warp == 8) {
     // ---------------- TMA producer ----------------
@@ -213,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(&sb.empty[u], ph ^ 1u, &sb.abort, p.status)) break;
         mbar_expect_tx(&sb.full[u], kUnit);
         uint8_t* dst = ring + u * kUnit;
-        const int krow = (j0 + tile) * BN;
+        const int krow = (j0 + tile_of(tile)) * BN;
         if (drop_first_copy && issued == 0 && blockIdx.x == 0) {
           // Test hook (attn_test_inject): the first CTA's first unit is
           // announced but never copied, so the MMA warp's wait runs out.
@@ -284,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // O += P[slot] V(tile): 8 MMAs of K = 16 keys, 4 per V unit.
     auto issue_pv = [&](int slot, int tile, bool first) -> bool {
-      const int k0 = (j0 + tile) * BN;
+      const int k0 = (j0 + tile_of(tile)) * BN;
       for (int hf = 0; hf < 2; ++hf) {
         const uint32_t vu = take();
         if (!vu) return false;
@@ -366,9 +446,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < n_tiles; ++i) {
       const int slot = i & 1;
       const uint32_t s_tm = tmem + lane_off + (slot ? C::kS1 : C::kS0);
-      const int k0 = (j0 + i) * BN + ch * kHalf;   // this thread's first key
+      const int k0 = (j0 + tile_of(i)) * BN + ch * kHalf;   // this thread's first key
       float mv[kHalf];
-      if (MASK) {
+      if (MASK && staged) {
+        // Staged values (keys past k_len hold whatever was there; they are hidden below).
+        const float4* ms4 = reinterpret_cast<const float4*>(m_s + (k0 - mbase));
+#pragma unroll
+        for (int j = 0; j < kHalf / 4; ++j) {
+          const float4 v4 = ms4[j];
+          mv[4 * j] = v4.x;
+          mv[4 * j + 1] = v4.y;
+          mv[4 * j + 2] = v4.z;
+          mv[4 * j + 3] = v4.w;
+        }
+      } else if (MASK) {
         // Mask values of this thread's 64 keys (vector loads when the slice is
         // in range and 16-byte aligned; hidden keys read as 0).  Issued before
         // the wait for S so their latency overlaps it.
@@ -565,12 +656,14 @@ int launch(const Problem& p, cudaStream_t st) {
   const int nqb = (p.Sq + BM - 1) / BM;
   const int64_t blocks = (int64_t)nqb * p.H * p.B;
   if (blocks > 0x7fffffff) return -1;
-  const int smem = Cfg<D>::kSmem + 1024;
+  const int smem = Cfg<D, MASK>::kSmem + 1024;
   auto kern = prefill_tc1_kernel<D, BF16, MASK>;
   cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, drop);
+  // A mask broadcast over heads and rows is staged in shared memory.
+  const int mask_stage = (MASK && p.m.hs == 0 && p.m.rs == 0) ? 1 : 0;
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, drop, mask_stage);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -245,3 +245,45 @@ def test_staged_broadcast_mask_batches_and_special_values(i):
     st = compare(o, lse, ref_o, ref_l, "bf16", "nan", c.name)
     assert st["nan_rows"] > 0
     assert attn.attn_device_status() == attn.ATTN_OK
+
+
+# ---- key tiles whose broadcast mask is -inf throughout are skipped -------------------------------
+
+DEAD = [
+    # head_dim, dtype, batch, q_len, k_len, causal, smooth softmax
+    (128, "bf16", 3, 300, 1100, False, False),
+    (64, "bf16", 2, 200, 700, True, False),
+    (256, "f16", 3, 130, 1000, False, False),
+    (256, "f16", 2, 200, 640, False, True),
+]
+
+
+@pytest.mark.parametrize("i", range(len(DEAD)))
+def test_fully_masked_key_tiles_match_the_oracle(i):
+    """A [B,1,1,K] mask with whole 128-key tiles at -inf (the first, one in the
+    middle, the last, partial), a NaN inside an otherwise -inf tile (the tile
+    stays: rows that see it are NaN), and one batch entry masked everywhere
+    (no tile left: a masked row, or O = 0 with the sink's LSE under smooth
+    softmax).  The head_dim-256 kernel skips the tiles of -inf; the result
+    matches the oracle on every kernel."""
+    D, dt, B, Sq, Sk, causal, smooth = DEAD[i]
+    r = np.random.default_rng(2100 + i)
+    mask = r.standard_normal((B, 1, 1, Sk)).astype(np.float32)
+    mask[r.random(mask.shape) < 0.1] = -np.inf
+    mask[0, 0, 0, :128] = -np.inf                # first tile
+    mask[0, 0, 0, 384:512] = -np.inf             # a middle tile
+    mask[0, 0, 0, (Sk // 128) * 128:] = -np.inf  # the partial last tile
+    mask[1, 0, 0, 128:384] = -np.inf             # two tiles ...
+    mask[1, 0, 0, 300] = np.nan                  # ... one of which keeps a NaN
+    mask[B - 1] = -np.inf                        # the last entry: nothing visible
+    c = wl.make_case(name=f"dead{i}", seed=2150 + i, dtype=dt, layout="bshd", batch=B, heads=4, kv_heads=2,
+                     q_len=Sq, k_len=Sk, head_dim=D, mask=mask, mask_kind="b11k", causal=causal,
+                     causal_offset=Sk - Sq if causal else None, smooth_softmax=smooth)
+    g = GpuCase(c).run()
+    o, lse, _ = g.outputs()
+    g.check_guards()
+    ref_o, ref_l = oracle_full(c)
+    st = compare(o, lse, ref_o, ref_l, dt, "nan", c.name)
+    if not smooth:
+        assert st["nan_rows"] >= 4 * Sq        # the last entry at least
+    assert attn.attn_device_status() == attn.ATTN_OK
