@@ -48,7 +48,7 @@ class attn_problem(ctypes.Structure):
                 ("k_lens_kind", ctypes.c_int32), ("softcap", ctypes.c_float),
                 ("smooth_softmax", ctypes.c_int32), ("head_sink", ctypes.c_void_p),
                 ("kv_dtype", ctypes.c_int32), ("kv_scale_kind", ctypes.c_int32),
-                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("key_splits", ctypes.c_int32)]
 
 
 class AttnError(RuntimeError):
@@ -193,6 +193,7 @@ def make_problem(d: dict) -> attn_problem:
                        else ATTN_KV_SCALE_TENSOR)
     p.k_scale = d.get("k_scale_ptr")          # device addresses of float32 scales (int8 caches)
     p.v_scale = d.get("v_scale_ptr")
+    p.key_splits = int(d.get("key_splits") or 0)   # attn_fwd key ranges: 0 = the library's plan
     return p
 
 
@@ -228,14 +229,15 @@ def _check(code, where):
 def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, mask=None, seg=None,
         k_lens=None, masked_rows="nan", return_lse=False, out=None, lse=None, stream=None,
         window_left=None, causal_align="fixed", k_lens_kind="count", softcap=0.0, smooth_softmax=False,
-        head_sink=None):
+        head_sink=None, key_splits=0):
     """O (and LSE) for torch CUDA tensors.  layout 'bshd': Q [B,Sq,H,D], K/V [B,Sk,G,D];
     'bhsd': Q [B,H,Sq,D], K/V [B,G,Sk,D].  mask: float32 broadcastable 4-D [B|1, H|1, Sq|1, Sk]
     with contiguous keys; seg: int32 [B, Sq] or [Sq]; k_lens: int32 [B].  window_left: left
     window of causal local attention (None = off); causal_align: 'fixed' (one offset) or
     'klens' (each entry's diagonal right-aligned to its key length); k_lens_kind: 'count' or
     'last_index' (ONNX seqlens_k, count minus one).  softcap: cap of the scaled scores (0 = off);
-    smooth_softmax / head_sink (float32 [H] CUDA tensor): the sink term of the denominator."""
+    smooth_softmax / head_sink (float32 [H] CUDA tensor): the sink term of the denominator.
+    key_splits: key ranges merged in range order (0 = the library's shape-only plan)."""
     torch = _torch()
     hd = 2 if layout == "bshd" else 1
     sd = 1 if layout == "bshd" else 2
@@ -248,7 +250,7 @@ def fwd(q, k, v, *, layout="bshd", causal=False, causal_offset=None, scale=0.0, 
              q_layout=_layout4(q, hd), k_layout=_layout4(k, hd), v_layout=_layout4(v, hd),
              o_layout=_layout4(out, hd), window_left=window_left, causal_align=causal_align,
              k_lens_kind=k_lens_kind, softcap=softcap, smooth_softmax=smooth_softmax,
-             head_sink_ptr=_ptr(head_sink))
+             head_sink_ptr=_ptr(head_sink), key_splits=key_splits)
     if mask is not None:
         if mask.dtype != torch.float32 or mask.dim() != 4 or mask.stride(3) != 1:
             raise ValueError("mask must be float32, 4-D, keys contiguous")

@@ -139,6 +139,7 @@ int check_problem(const attn_problem* p) {
   if (p->kv_dtype != ATTN_KV_AS_Q && p->kv_dtype != ATTN_KV_INT8) return ATTN_ERR_INVALID_ARG;
   if (p->kv_scale_kind != ATTN_KV_SCALE_TENSOR && p->kv_scale_kind != ATTN_KV_SCALE_CHANNEL)
     return ATTN_ERR_INVALID_ARG;
+  if (p->key_splits < 0) return ATTN_ERR_INVALID_ARG;
   if (p->kv_dtype == ATTN_KV_INT8) {
     if (!p->k_scale || !p->v_scale) return ATTN_ERR_INVALID_ARG;
     if (!aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)) return ATTN_ERR_ALIGNMENT;
@@ -243,6 +244,40 @@ void decode_plan(const attn_problem* p, int* n_splits, int* split_len) {
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Prefill key-range plan ("Attention", section "Accuracy at long key
+// lengths": ranges cut by the shape, at most 16, merged in range order).  A
+// problem with fewer blocks of query rows than two per SM of a GB300 (304;
+// 256 rows a block for head_dim <= 128, 128 above) and a long key axis gets
+// ceil(304 / blocks) ranges, at most 16 and at most one per 1024 keys, so
+// that each range's CTA has at least eight 128-key tiles to amortise its
+// fixed cost; key_splits > 0 asks for a count instead.  Range lengths are a
+// multiple of 128 keys (a key tile).
+constexpr int kFillBlocks = 304;
+constexpr int kMaxRanges = 16;
+
+void fwd_plan(const attn_problem* p, int* n_splits, int* split_len) {
+  const int64_t Sk = p->k_len;
+  *n_splits = 1;
+  *split_len = Sk > 0 ? (int)Sk : 1;
+  if (Sk <= 0 || p->q_len <= 0 || p->batch <= 0) return;
+  int64_t n;
+  if (p->key_splits > 0) {
+    n = p->key_splits < kMaxRanges ? p->key_splits : kMaxRanges;
+  } else {
+    const int rows = p->head_dim <= 128 ? 256 : 128;
+    const int64_t blocks = (int64_t)((p->q_len + rows - 1) / rows) * p->heads * p->batch;
+    if (blocks >= kFillBlocks) return;
+    n = (kFillBlocks + blocks - 1) / blocks;
+    n = n < kMaxRanges ? n : kMaxRanges;
+    n = n < Sk / 1024 ? n : Sk / 1024;
+  }
+  if (n < 2) return;
+  int64_t len = (Sk + n - 1) / n;
+  len = (len + 127) / 128 * 128;
+  *split_len = (int)len;
+  *n_splits = (int)((Sk + len - 1) / len);
+}
+
 size_t decode_ws_bytes(const attn_problem* p, int n_splits) {
   const size_t rows = (size_t)p->batch * p->heads * p->q_len;
   return round256(rows * n_splits * p->head_dim * sizeof(float)) + round256(rows * n_splits * sizeof(float));
@@ -299,7 +334,9 @@ extern "C" {
 
 size_t attn_fwd_workspace_size(const attn_problem* p) {
   if (check_problem(p) != ATTN_OK) return 0;
-  return 0;
+  int n = 1, len = 1;
+  fwd_plan(p, &n, &len);
+  return n > 1 ? decode_ws_bytes(p, n) : 0;
 }
 
 int attn_fwd(const attn_problem* p, const void* q, const void* k, const void* v, void* o, const float* mask,
@@ -310,18 +347,35 @@ int attn_fwd(const attn_problem* p, const void* q, const void* k, const void* v,
   if (p->batch == 0 || p->q_len == 0) return ATTN_OK;
   rc = check_pointers(p, q, k, v, o, mask, seg, k_lens, lse);
   if (rc) return rc;
-  (void)workspace;
-  (void)workspace_bytes;
+  int n_splits = 1, split_len = 1;
+  fwd_plan(p, &n_splits, &split_len);
+  Split s{1, p->k_len > 0 ? p->k_len : 1, nullptr, nullptr};
+  if (n_splits > 1) {
+    const size_t need = decode_ws_bytes(p, n_splits);
+    if (workspace && workspace_bytes >= need && aligned(workspace, 256)) {
+      const size_t rows = (size_t)p->batch * p->heads * p->q_len;
+      s.n_splits = n_splits;
+      s.split_len = split_len;
+      s.part_o = static_cast<float*>(workspace);
+      s.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            round256(rows * n_splits * p->head_dim * sizeof(float)));
+    } else if (p->key_splits > 1) {
+      return workspace && workspace_bytes >= need ? ATTN_ERR_ALIGNMENT : ATTN_ERR_WORKSPACE;
+    }
+  }
   int* status = nullptr;
   rc = status_ptr(&status);
   if (rc) return rc;
   Problem r = resolve(p, q, k, v, o, mask, seg, k_lens, lse, status);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int used = 0;
-  rc = prefill_tc_try(r, st, &used);
-  if (rc || used) return rc;
-  Split s{1, p->k_len > 0 ? p->k_len : 1, nullptr, nullptr};
-  return from_cuda(launch_simt(r, s, st));
+  rc = prefill_tc_try(r, s, st, &used);
+  if (rc) return rc;
+  if (!used) {
+    rc = from_cuda(launch_simt(r, s, st));
+    if (rc) return rc;
+  }
+  return s.n_splits > 1 ? from_cuda(launch_combine(r, s, p->dtype, st)) : ATTN_OK;
 }
 
 size_t attn_decode_workspace_size(const attn_problem* p) {
@@ -403,6 +457,6 @@ int attn_test_inject(int32_t fault) {
   return ATTN_OK;
 }
 
-int attn_version(void) { return 240; }
+int attn_version(void) { return 250; }
 
 }  // extern "C"

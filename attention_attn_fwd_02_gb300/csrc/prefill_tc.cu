@@ -85,7 +85,7 @@ template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
-                      const int mask_bcast, const int drop_first_copy) {
+                      const int mask_bcast, const int drop_first_copy, const Split sp) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -102,10 +102,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (block L covers query block n_qblocks-1-L/(H*B)).  Otherwise every block
   // does the same work, and the query blocks of one (batch, head) run side by
   // side so that its K and V come from DRAM once and from L2 after that.
+  // With key ranges (sp.n_splits > 1) the ranges of one query block are
+  // adjacent in the launch order and each CTA takes one.
   const int HB = p.H * p.B;
   const bool lpt = p.causal || p.seg != nullptr;
-  const int hb = lpt ? (int)(blockIdx.x % HB) : (int)(blockIdx.x / n_qblocks);
-  const int qb = lpt ? n_qblocks - 1 - (int)(blockIdx.x / HB) : (int)(blockIdx.x % n_qblocks);
+  const int blk = sp.n_splits > 1 ? (int)(blockIdx.x / sp.n_splits) : (int)blockIdx.x;
+  const int64_t kr0 = sp.n_splits > 1 ? (int64_t)(blockIdx.x % sp.n_splits) * sp.split_len : 0;
+  const int64_t kr1 = sp.n_splits > 1 ? min((int64_t)p.Sk, kr0 + sp.split_len) : (int64_t)p.Sk;
+  const int hb = lpt ? blk % HB : blk / n_qblocks;
+  const int qb = lpt ? n_qblocks - 1 - blk / HB : blk % n_qblocks;
   const int h = hb % p.H, b = hb / p.H;
   const int g = h / p.qpg;
   const int q0 = qb * 2 * BM;
@@ -146,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8 && qrow < p.Sq) {
     int64_t lo64, hi64;
     row_range(p, b, qrow, lo64, hi64);
+    lo64 = max(lo64, kr0);
+    hi64 = min(hi64, kr1);
     lo = (int)lo64;
     hi = (int)(hi64 > lo64 ? hi64 : lo64);
   }
@@ -168,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (last >= q0) {
       row_range(p, b, last, l64, h64);
       row_range(p, b, q0, f_lo, f_hi);
+      f_lo = max(f_lo, kr0);
+      h64 = min(h64, kr1);
     }
     lo_u = (int)f_lo;
     hi_u = h64 > f_lo ? (int)h64 : -1;
@@ -527,8 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       fence_after();
       const bool valid = qrow < p.Sq;
-      // The sink logit joins the denominator (and rescales the accumulated O).
-      const float o_mul = p.sink_on ? fold_sink<true>(m_ref, l, sink_logit(p, h) * kLog2e) : 1.f;
+      // The sink logit joins the denominator (and rescales the accumulated O);
+      // with key ranges the merge adds it once.
+      const float o_mul = p.sink_on && sp.n_splits == 1 ? fold_sink<true>(m_ref, l, sink_logit(p, h) * kLog2e) : 1.f;
       const bool hidden_row = (l == 0.f);         // no visible key; a NaN l stays a NaN row
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* orow = valid ? static_cast<T*>(p.O) + p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs +
@@ -536,32 +546,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                       : nullptr;
       const float inv = o_mul / l;
       const float fill = p.masked_zero ? 0.f : NAN;
+      if (sp.n_splits > 1) {
+        // This key range's partial: O / l in float32 and its LSE (-inf when
+        // the range has no visible key; the merge then gives it no weight).
+        const int split = (int)(blockIdx.x % sp.n_splits);
+        const int64_t prow = ((int64_t)b * p.H + h) * p.Sq + qrow;
+        float4* po = reinterpret_cast<float4*>(sp.part_o + (prow * sp.n_splits + split) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(o_tm + c * 32, o);
-          tmem_ld_wait_regs<1>(o);
-        } else {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(o_tm + c * 32, o);
+            tmem_ld_wait_regs<1>(o);
+          }
+          if (valid && !hidden_row) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
+            for (int e = 0; e < 32; e += 4)
+              po[c * 8 + e / 4] = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                              __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+          }
         }
-        uint32_t w[16];
+        if (valid) sp.part_lse[prow * sp.n_splits + split] = hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
+      } else {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float a = hidden_row ? fill : __uint_as_float(o[e]) * inv;
-          float bb = hidden_row ? fill : __uint_as_float(o[e + 1]) * inv;
-          w[e / 2] = pack2<BF16>(a, bb);
-        }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(o_tm + c * 32, o);
+            tmem_ld_wait_regs<1>(o);
+          } else {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float a = hidden_row ? fill : __uint_as_float(o[e]) * inv;
+            float bb = hidden_row ? fill : __uint_as_float(o[e + 1]) * inv;
+            w[e / 2] = pack2<BF16>(a, bb);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          }
         }
+        if (valid && p.lse)
+          p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
+              hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
       }
-      if (valid && p.lse)
-        p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
-            hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
     }
   }
 
@@ -576,14 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---- host side -----------------------------------------------------------------------
 
 template <int D, bool BF16, bool MASK>
-int launch(const Problem& p, cudaStream_t st) {
+int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!tma_map_bhsd(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q, BM) ||
       !tma_map_bhsd(&mk, p.K, p.dtype, D, p.Sk, p.G, p.B, p.k, BN) ||
       !tma_map_bhsd(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v, BN))
     return -1;  // not describable: caller falls back
   const int nqb = (p.Sq + 2 * BM - 1) / (2 * BM);
-  const int64_t blocks = (int64_t)nqb * p.H * p.B;
+  const int64_t blocks = (int64_t)nqb * p.H * p.B * sp.n_splits;
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D>::kSmem + 1024;
   auto kern = prefill_tc_kernel<D, BF16, MASK>;
@@ -605,20 +638,20 @@ int launch(const Problem& p, cudaStream_t st) {
                              ? 1
                              : 0;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, mask_bcast, drop);
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, mask_bcast, drop, sp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 template <int D>
-int launch_d(const Problem& p, cudaStream_t st) {
+int launch_d(const Problem& p, const Split& sp, cudaStream_t st) {
   const bool m = p.M != nullptr;
-  if (p.dtype == ATTN_BF16) return m ? launch<D, true, true>(p, st) : launch<D, true, false>(p, st);
-  return m ? launch<D, false, true>(p, st) : launch<D, false, false>(p, st);
+  if (p.dtype == ATTN_BF16) return m ? launch<D, true, true>(p, sp, st) : launch<D, true, false>(p, sp, st);
+  return m ? launch<D, false, true>(p, sp, st) : launch<D, false, false>(p, sp, st);
 }
 
 }  // namespace tc
 
-int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
+int prefill_tc_try(const Problem& p, const Split& sp, cudaStream_t st, int* used) {
   *used = 0;
   if (p.dtype != ATTN_BF16 && p.dtype != ATTN_F16) return ATTN_OK;
   if (p.kv_int8) return ATTN_OK;  // int8 caches: the CUDA-core path
@@ -630,7 +663,8 @@ int prefill_tc_try(const Problem& p, cudaStream_t st, int* used) {
   if (!tma_layout_ok(p.Q, p.q, p.Sq, p.H, p.B) || !tma_layout_ok(p.K, p.k, p.Sk, p.G, p.B) ||
       !tma_layout_ok(p.V, p.v, p.Sk, p.G, p.B) || !tma_layout_ok(p.O, p.o, p.Sq, p.H, p.B))
     return ATTN_OK;
-  const int rc = p.D == 256 ? prefill_tc1_launch(p, st) : (p.D == 64 ? tc::launch_d<64>(p, st) : tc::launch_d<128>(p, st));
+  const int rc = p.D == 256 ? prefill_tc1_launch(p, sp, st)
+                            : (p.D == 64 ? tc::launch_d<64>(p, sp, st) : tc::launch_d<128>(p, sp, st));
   if (rc < 0) return ATTN_OK;  // tensor map refused: generic path
   *used = 1;
   return rc;

@@ -135,7 +135,7 @@ template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
-                       const int drop_first_copy, const int mask_stage) {
+                       const int drop_first_copy, const int mask_stage, const Split sp) {
   using C = Cfg<D, MASK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -149,10 +149,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (block L covers query block n_qblocks-1-L/(H*B)).  Otherwise every block
   // does the same work, and the query blocks of one (batch, head) run side by
   // side so that its K and V come from DRAM once and from L2 after that.
+  // With key ranges (sp.n_splits > 1) the ranges of one query block are
+  // adjacent in the launch order and each CTA takes one.
   const int HB = p.H * p.B;
   const bool lpt = p.causal || p.seg != nullptr;
-  const int hb = lpt ? (int)(blockIdx.x % HB) : (int)(blockIdx.x / n_qblocks);
-  const int qb = lpt ? n_qblocks - 1 - (int)(blockIdx.x / HB) : (int)(blockIdx.x % n_qblocks);
+  const int blk = sp.n_splits > 1 ? (int)(blockIdx.x / sp.n_splits) : (int)blockIdx.x;
+  const int64_t kr0 = sp.n_splits > 1 ? (int64_t)(blockIdx.x % sp.n_splits) * sp.split_len : 0;
+  const int64_t kr1 = sp.n_splits > 1 ? min((int64_t)p.Sk, kr0 + sp.split_len) : (int64_t)p.Sk;
+  const int hb = lpt ? blk % HB : blk / n_qblocks;
+  const int qb = lpt ? n_qblocks - 1 - blk / HB : blk % n_qblocks;
   const int h = hb % p.H, b = hb / p.H;
   const int g = h / p.qpg;
   const int q0 = qb * BM;
@@ -191,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 8 && qrow < p.Sq) {
     int64_t lo64, hi64;
     row_range(p, b, qrow, lo64, hi64);
+    lo64 = max(lo64, kr0);
+    hi64 = min(hi64, kr1);
     lo = (int)lo64;
     hi = (int)(hi64 > lo64 ? hi64 : lo64);
   }
@@ -600,8 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       fence_after();
       const bool valid = qrow < p.Sq;
-      // The sink logit joins the denominator (and rescales the accumulated O).
-      const float o_mul = p.sink_on ? fold_sink<true>(m_ref, l, sink_logit(p, h) * kLog2e) : 1.f;
+      // The sink logit joins the denominator (and rescales the accumulated O);
+      // with key ranges the merge adds it once.
+      const float o_mul = p.sink_on && sp.n_splits == 1 ? fold_sink<true>(m_ref, l, sink_logit(p, h) * kLog2e) : 1.f;
       const bool hidden_row = (l == 0.f);  // no visible key; a NaN l stays a NaN row
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
       T* orow = valid ? static_cast<T*>(p.O) + p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs +
@@ -609,32 +617,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                       : nullptr;
       const float inv = o_mul / l;
       const float fill = p.masked_zero ? 0.f : NAN;
+      if (sp.n_splits > 1) {
+        // This key range's partial: O / l in float32 (each thread its half of
+        // the columns) and its LSE (-inf when the range has no visible key).
+        const int split = (int)(blockIdx.x % sp.n_splits);
+        const int64_t prow = ((int64_t)b * p.H + h) * p.Sq + qrow;
+        float4* po = reinterpret_cast<float4*>(sp.part_o + (prow * sp.n_splits + split) * D + ch * (D / 2));
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(o_tm + c * 32, o);
-          tmem_ld_wait_regs<1>(o);
-        } else {
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(o_tm + c * 32, o);
+            tmem_ld_wait_regs<1>(o);
+          }
+          if (valid && !hidden_row) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
+            for (int e = 0; e < 32; e += 4)
+              po[c * 8 + e / 4] = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                              __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+          }
         }
-        uint32_t w[16];
+        if (valid && ch == 0)
+          sp.part_lse[prow * sp.n_splits + split] = hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
+      } else {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float a = hidden_row ? fill : __uint_as_float(o[e]) * inv;
-          const float bb = hidden_row ? fill : __uint_as_float(o[e + 1]) * inv;
-          w[e / 2] = pack2<BF16>(a, bb);
-        }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(o_tm + c * 32, o);
+            tmem_ld_wait_regs<1>(o);
+          } else {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float a = hidden_row ? fill : __uint_as_float(o[e]) * inv;
+            const float bb = hidden_row ? fill : __uint_as_float(o[e + 1]) * inv;
+            w[e / 2] = pack2<BF16>(a, bb);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          }
         }
+        if (valid && p.lse && ch == 0)
+          p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
+              hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
       }
-      if (valid && p.lse && ch == 0)
-        p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
-            hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
     }
   }
 
@@ -647,14 +679,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool BF16, bool MASK>
-int launch(const Problem& p, cudaStream_t st) {
+int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!tma_map_bhsd(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q, BM) ||
       !tma_map_bhsd(&mk, p.K, p.dtype, D, p.Sk, p.G, p.B, p.k, BN) ||
       !tma_map_bhsd(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v, BN / 2))
     return -1;  // not describable: caller falls back
   const int nqb = (p.Sq + BM - 1) / BM;
-  const int64_t blocks = (int64_t)nqb * p.H * p.B;
+  const int64_t blocks = (int64_t)nqb * p.H * p.B * sp.n_splits;
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D, MASK>::kSmem + 1024;
   auto kern = prefill_tc1_kernel<D, BF16, MASK>;
@@ -663,17 +695,18 @@ int launch(const Problem& p, cudaStream_t st) {
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
   // A mask broadcast over heads and rows is staged in shared memory.
   const int mask_stage = (MASK && p.m.hs == 0 && p.m.rs == 0) ? 1 : 0;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, drop, mask_stage);
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, drop, mask_stage, sp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace tc1
 
-int prefill_tc1_launch(const Problem& p, cudaStream_t st) {
+int prefill_tc1_launch(const Problem& p, const Split& sp, cudaStream_t st) {
   const bool m = p.M != nullptr;
   if (p.D != 256) return -1;
-  if (p.dtype == ATTN_BF16) return m ? tc1::launch<256, true, true>(p, st) : tc1::launch<256, true, false>(p, st);
-  return m ? tc1::launch<256, false, true>(p, st) : tc1::launch<256, false, false>(p, st);
+  if (p.dtype == ATTN_BF16)
+    return m ? tc1::launch<256, true, true>(p, sp, st) : tc1::launch<256, true, false>(p, sp, st);
+  return m ? tc1::launch<256, false, true>(p, sp, st) : tc1::launch<256, false, false>(p, sp, st);
 }
 
 }  // namespace attn

@@ -275,6 +275,15 @@ def masked_gqa_bf16(seed: int = 3, batch: int = 2, seq: int = 4096, heads: int =
                      causal=False, causal_offset=None, value_scale=0.5, mask=mask, mask_kind="b11k")
 
 
+def short_query_cross_bf16(seed: int = 6, batch: int = 1, heads: int = 32, kv_heads: int = 8, q_len: int = 64,
+                           k_len: int = 8192) -> Case:
+    """A few queries against a long key axis (bf16, head dim 128, head-first, non-causal): too few blocks
+    of query rows to fill the GPU, so the keys are cut into ranges (a context measurement of the split)."""
+    return make_case(name=f"short_query_cross_bf16_b{batch}_h{heads}_kv{kv_heads}_q{q_len}_k{k_len}_d128",
+                     seed=seed, dtype="bf16", layout="bhsd", batch=batch, heads=heads, kv_heads=kv_heads,
+                     q_len=q_len, k_len=k_len, head_dim=128, value_scale=0.5)
+
+
 def decode_bnsh_bf16(seed: int = 4, batch: int = 64, capacity: int = 8192, heads: int = 32,
                      kv_heads: int = 8, min_len: int = 512) -> Case:
     """Batched single-query decode over a BNSH cache [B, 8, capacity, 128], lengths uniform in [512, capacity]."""

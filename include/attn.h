@@ -164,17 +164,37 @@ typedef struct {
   int32_t kv_scale_kind;           /* ATTN_KV_SCALE_TENSOR / ATTN_KV_SCALE_CHANNEL */
   const float* k_scale;            /* DEVICE float32 scales, required with ATTN_KV_INT8 */
   const float* v_scale;
+  /* Key-range split of attn_fwd ("Attention", section "Accuracy at long key
+   * lengths": the keys are cut into ranges by the shape, each range gives a
+   * partial (LSE, O), and the partials are merged in range order).  0: the
+   * library's plan (ranges only when the problem has too few query blocks to
+   * fill the GPU and at least 2048 keys, see attn_fwd_workspace_size);
+   * n >= 1: exactly min(n, 16) ranges of equal length (a multiple of 128
+   * keys), the last one shorter.  attn_decode ignores it. */
+  int32_t key_splits;
 } attn_problem;
 
-/* Bytes of device workspace attn_fwd needs for this problem (0 when none).
- * Returns 0 also for an invalid problem; attn_fwd then reports the error. */
+/* Bytes of device workspace attn_fwd needs for this problem (0 when none):
+ * the partial results of its key ranges (float32 [B*H*q_len][ranges][head_dim]
+ * and [B*H*q_len][ranges], each 256-byte aligned).  The plan depends on the
+ * shape only: without key_splits the keys are cut into ranges when the
+ * problem has fewer than 304 blocks of query rows (256 rows a block for
+ * head_dim <= 128, 128 above; two blocks per SM of a GB300) and at least
+ * 2048 keys: ceil(304 / blocks) ranges, at most 16 and at most one per 1024
+ * keys.  Returns 0 also for an invalid problem; attn_fwd then reports the
+ * error. */
 ATTN_API size_t attn_fwd_workspace_size(const attn_problem* p);
 
 /* Prefill / full forward.  q, k, v, o: device pointers in p->dtype laid out
  * by p->q, p->k, p->v, p->o.  mask (nullable): float32, strides p->mask.
  * seg (nullable): int32 segment starts.  k_lens (nullable): int32 [batch]
  * key counts.  lse (nullable): float32 output.  workspace: device scratch of
- * at least attn_fwd_workspace_size(p) bytes (NULL when that is 0).
+ * attn_fwd_workspace_size(p) bytes, 256-byte aligned.  When the plan cuts the
+ * keys into ranges, a pass writes each range's partial into the workspace and
+ * a second kernel merges them in range order; with a smaller workspace (NULL
+ * included) the call runs without ranges, unless p->key_splits > 1 asks for
+ * them, which returns ATTN_ERR_WORKSPACE.  The two forms agree within
+ * rounding (the sums run in another order); each is deterministic.
  * batch == 0 or q_len == 0 is a no-op returning ATTN_OK. */
 ATTN_API int attn_fwd(const attn_problem* p, const void* q, const void* k, const void* v, void* o,
              const float* mask, const int32_t* seg, const int32_t* k_lens, float* lse,

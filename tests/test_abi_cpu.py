@@ -49,15 +49,15 @@ def test_struct_layout_matches_c(tmp_path):
                    ' offsetof(attn_problem, lse_head_stride)); printf("%zu %zu %zu\\n",'
                    ' offsetof(attn_problem, window_left), offsetof(attn_problem, causal_align),'
                    ' offsetof(attn_problem, k_lens_kind)); printf("%zu %zu\\n", offsetof(attn_problem, softcap),'
-                   ' offsetof(attn_problem, head_sink)); printf("%zu %zu\\n", offsetof(attn_problem, kv_dtype),'
-                   ' offsetof(attn_problem, v_scale)); return 0;}\n')
+                   ' offsetof(attn_problem, head_sink)); printf("%zu %zu %zu\\n", offsetof(attn_problem, kv_dtype),'
+                   ' offsetof(attn_problem, v_scale), offsetof(attn_problem, key_splits)); return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.run(["gcc", str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     P = attn.attn_problem
     want = [ctypes.sizeof(P), P.causal_offset.offset, P.q.offset, P.mask.offset, P.seg_batch_stride.offset,
             P.lse_head_stride.offset, P.window_left.offset, P.causal_align.offset, P.k_lens_kind.offset,
-            P.softcap.offset, P.head_sink.offset, P.kv_dtype.offset, P.v_scale.offset]
+            P.softcap.offset, P.head_sink.offset, P.kv_dtype.offset, P.v_scale.offset, P.key_splits.offset]
     assert got == want
 
 
@@ -174,6 +174,52 @@ def test_decode_workspace_follows_the_range_plan(L, k_len, batch, kv_heads, int8
     assert attn.attn_decode_workspace_size(base_problem(**kw)) == _r256(rows * n * D * 4) + _r256(rows * n * 4)
 
 
+def _fwd_ranges(B, H, Sq, Sk, D, key_splits):
+    """The prefill key-range plan restated from the header: ranges only with
+    fewer than 304 blocks of query rows and a long key axis."""
+    if key_splits > 0:
+        n = min(key_splits, 16)
+    else:
+        rows = 256 if D <= 128 else 128
+        blocks = -(-Sq // rows) * H * B
+        if blocks >= 304:
+            return 1
+        n = min(-(-304 // blocks), 16, Sk // 1024)
+    if n < 2:
+        return 1
+    length = -(-(-(-Sk // n)) // 128) * 128
+    return -(-Sk // length)
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,D,ks", [
+    (1, 32, 64, 8192, 128, 0), (4, 12, 1024, 1024, 64, 0), (4, 12, 1024, 1024, 64, 4), (2, 32, 4096, 4096, 128, 0),
+    (1, 4, 100, 5000, 256, 0), (1, 1, 1, 3000, 128, 0), (2, 2, 16, 1500, 64, 0), (1, 2, 8, 8, 64, 3),
+    (1, 8, 300, 20000, 128, 40)])
+def test_fwd_workspace_follows_the_range_plan(L, B, H, Sq, Sk, D, ks):
+    """attn_fwd's workspace holds one partial row and one LSE per (batch, head,
+    query row, key range) when the shape-only plan (or key_splits) cuts the keys."""
+    G = H
+    kw = dict(batch=B, heads=H, kv_heads=G, q_len=Sq, k_len=Sk, head_dim=D, key_splits=ks,
+              q_layout=(0, H * Sq * D, Sq * D, D), o_layout=(0, H * Sq * D, Sq * D, D),
+              k_layout=(0, G * Sk * D, Sk * D, D), v_layout=(0, G * Sk * D, Sk * D, D))
+    n = _fwd_ranges(B, H, Sq, Sk, D, ks)
+    rows = B * H * Sq
+    want = 0 if n == 1 else _r256(rows * n * D * 4) + _r256(rows * n * 4)
+    assert attn.attn_fwd_workspace_size(base_problem(**kw)) == want
+
+
+def test_fwd_forced_ranges_need_the_workspace(L):
+    """key_splits > 1 with no workspace is refused before any launch; a negative count is invalid."""
+    kw = dict(batch=1, heads=2, kv_heads=2, q_len=8, k_len=1000, head_dim=64,
+              q_layout=(0, 2 * 8 * 64, 8 * 64, 64), o_layout=(0, 2 * 8 * 64, 8 * 64, 64),
+              k_layout=(0, 2 * 1000 * 64, 1000 * 64, 64), v_layout=(0, 2 * 1000 * 64, 1000 * 64, 64))
+    p = base_problem(key_splits=4, **kw)
+    assert attn.attn_fwd_workspace_size(p) > 0
+    assert attn.attn_fwd(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None, 0, None) == attn.ATTN_ERR_WORKSPACE
+    p = base_problem(key_splits=-1, **kw)
+    assert attn.attn_fwd(p, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
+
+
 def test_combine_checks(L):
     assert attn.attn_combine(4, 0, 64, None, None, 0, None, 64, None, 0, None) == 0
     assert attn.attn_combine(4, 3, 0, FAKE, FAKE, 0, FAKE, 64, None, 0, None) == attn.ATTN_ERR_INVALID_ARG
@@ -195,7 +241,7 @@ def test_status_strings_and_version(L):
     for code in range(7):
         assert attn.status_string(code) and attn.status_string(code) != "unknown status"
     assert attn.status_string(99) == "unknown status"
-    assert attn.attn_version() >= 240
+    assert attn.attn_version() >= 250
 
 
 def test_test_inject_checks(L):

@@ -287,3 +287,75 @@ def test_fully_masked_key_tiles_match_the_oracle(i):
     if not smooth:
         assert st["nan_rows"] >= 4 * Sq        # the last entry at least
     assert attn.attn_device_status() == attn.ATTN_OK
+
+
+# ---- key ranges merged in range order --------------------------------------------------------------
+
+def _split_mask(seed, B, Sk):
+    """N(0,1) mask with 10% of keys -inf and the last batch entry -inf throughout."""
+    r = np.random.default_rng(seed)
+    m = r.standard_normal((B, 1, 1, Sk)).astype(np.float32)
+    m[r.random(m.shape) < 0.1] = -np.inf
+    m[B - 1] = -np.inf
+    return m
+
+
+def _with_ranges(case, n):
+    case.problem = dict(case.problem, key_splits=n)
+    return case
+
+
+SPLIT = {
+    # the causal GQA workload with documents, its keys forced into 4 ranges (many of them empty for a block)
+    "gqa_doc_4_ranges": lambda: _with_ranges(wl.gqa_doc_causal_bf16(), 4),
+    # 64 queries against 8192 keys: the automatic plan cuts 8 ranges
+    "short_query_auto": lambda: wl.short_query_cross_bf16(batch=1, heads=8, kv_heads=2),
+    # head_dim 256 with a broadcast mask and a fully masked entry, automatic ranges
+    "d256_mask_auto": lambda: wl.make_case(
+        name="split256", seed=2201, dtype="f16", layout="bshd", batch=2, heads=4, kv_heads=2, q_len=100, k_len=5000,
+        head_dim=256, mask=_split_mask(2202, 2, 5000), mask_kind="b11k", masked_rows="zero"),
+    # causal bound right-aligned to per-entry key lengths with a sink, 5 forced ranges
+    "causal_klens_sink": lambda: _with_ranges(wl.make_case(
+        name="splitks", seed=2204, dtype="bf16", layout="bhsd", batch=3, heads=4, kv_heads=1, q_len=200, k_len=3000,
+        head_dim=128, causal=True, causal_align="klens", k_lens=np.array([3000, 1700, 0], dtype=np.int32),
+        head_sink=np.array([0.5, -1.0, 2.0, 0.0], dtype=np.float32)), 5),
+    # float32 on the CUDA-core path, 3 forced ranges
+    "f32_generic": lambda: _with_ranges(wl.make_case(
+        name="split32", seed=2205, dtype="f32", batch=1, heads=2, q_len=40, k_len=700, head_dim=32, causal=True), 3),
+}
+
+
+@pytest.mark.parametrize("name", list(SPLIT))
+def test_key_ranges_merged_in_range_order_match_the_oracle(name):
+    """attn_fwd with its keys cut into ranges: each range's partial (O / l and
+    LSE) goes to the workspace and the merge combines them in range order; O
+    and LSE match the oracle, NaN / masked rows included."""
+    c = SPLIT[name]()
+    g = GpuCase(c)
+    assert attn.attn_fwd_workspace_size(g.prob) > 0, "the plan should cut this problem into ranges"
+    g.run()
+    o, lse, _ = g.outputs()
+    g.check_guards()
+    ref_o, ref_l = oracle_full(c)
+    compare(o, lse, ref_o, ref_l, c.problem["dtype"], c.problem["masked_rows"], name)
+    assert attn.attn_device_status() == attn.ATTN_OK
+
+
+def test_key_ranges_with_a_nan_score_make_the_row_nan():
+    """A +inf mask entry inside one range makes exactly the rows that see it NaN after the merge."""
+    B, H, Sq, Sk = 1, 2, 64, 4096
+    mask = np.zeros((B, 1, 1, Sk), dtype=np.float32)
+    mask[0, 0, 0, 3000] = np.inf
+    c = wl.make_case(name="split_inf", seed=2210, dtype="bf16", layout="bhsd", batch=B, heads=H, q_len=Sq, k_len=Sk,
+                     head_dim=64, mask=mask, mask_kind="b11k", causal=True, causal_offset=2990)
+    g = GpuCase(c)
+    assert attn.attn_fwd_workspace_size(g.prob) > 0
+    st, _ = run_split_compare(g, c)
+    assert st["nan_rows"] == H * (Sq - 10)
+
+
+def run_split_compare(g, c):
+    g.run()
+    o, lse, _ = g.outputs()
+    ref_o, ref_l = oracle_full(c)
+    return compare(o, lse, ref_o, ref_l, c.problem["dtype"], c.problem["masked_rows"], c.name), g
