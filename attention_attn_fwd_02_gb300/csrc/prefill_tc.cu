@@ -168,15 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ends of a row's range are non-decreasing in the row (the window's left end
   // moves with the diagonal), so [lo of the first row, hi of the last row)
   // covers the union; otherwise reduce over rows.
-  int lo_u, hi_u;
+  // hi_0: the end of query tile 0's visible keys (without segment starts);
+  // under a causal bound tile 0 stops one key tile short of tile 1.
+  int lo_u, hi_u, hi_0 = 0x7fffffff;
   if (p.seg == nullptr) {
     const int last = min(q0 + 2 * BM, p.Sq) - 1;
-    int64_t l64 = 0, h64 = 0, f_lo = 0, f_hi = 0;
+    int64_t l64 = 0, h64 = 0, f_lo = 0, f_hi = 0, t_lo = 0, t_hi = 0;
     if (last >= q0) {
       row_range(p, b, last, l64, h64);
       row_range(p, b, q0, f_lo, f_hi);
+      row_range(p, b, min(q0 + BM, p.Sq) - 1, t_lo, t_hi);
       f_lo = max(f_lo, kr0);
       h64 = min(h64, kr1);
+      hi_0 = (int)min(t_hi, kr1);
     }
     lo_u = (int)f_lo;
     hi_u = h64 > f_lo ? (int)h64 : -1;
@@ -193,6 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool any = hi_u > lo_u;
   const int j0 = any ? lo_u / BN : 0;
   const int n_tiles = any ? (hi_u + BN - 1) / BN - j0 : 0;
+  // Key tiles of query tile 0: a prefix of the CTA's tiles (tile 1 sees at
+  // least as far), so the key tiles beyond its last visible key are not
+  // computed for it.
+  const int n0 = hi_0 >= hi_u ? n_tiles : (hi_0 > lo_u ? (hi_0 + BN - 1) / BN - j0 : 0);
 
   // Registers move from the producer warpgroup to the softmax warpgroups.
   // Each role sets its own count inside its branch, so no code after the
@@ -277,8 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Prologue: S0 and S1 of tile 0.
     if (ok) ok = wait_warp(&sb.k_full[0], 0, &sb.abort, p.status);
     if (ok) {
-      issue_qk(0, 0);
-      mma_commit_w(&sb.s_full[0]);
+      if (n0 > 0) {
+        issue_qk(0, 0);
+        mma_commit_w(&sb.s_full[0]);
+      }
       issue_qk(1, 0);
       mma_commit_w(&sb.s_full[1]);
       mma_commit_w(&sb.k_empty[0]);
@@ -289,9 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
       const int k0 = (j0 + i) * BN;
       const bool more = i + 1 < n_tiles;
+      const bool has0 = i < n0, more0 = i + 1 < n0;
       const int s1 = (i + 1) % C::kStages;
       const uint32_t ph1 = (uint32_t)((i + 1) / C::kStages) & 1u;
-      bool rp0 = mbar_test(&sb.p_full[0], (uint32_t)i & 1u);
+      bool rp0 = !has0 || mbar_test(&sb.p_full[0], (uint32_t)i & 1u);
       if (!(ok = wait_ready(rv, &sb.v_full[s], ph, &sb.abort, p.status))) break;
       // Zero the V rows of keys no row of this CTA sees (they may hold anything).
       if (k0 < lo_u || k0 + BN > hi_u) {
@@ -310,14 +321,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool rk = !more || mbar_test(&sb.k_full[s1], ph1);
       // Query tile 0: P0 V, then the next S0.
-      if (!(ok = wait_ready(rp0, &sb.p_full[0], (uint32_t)i & 1u, &sb.abort, p.status))) break;
-      issue_pv(0, s, i == 0);
-      mma_commit_w(&sb.o_done[0]);
+      if (has0) {
+        if (!(ok = wait_ready(rp0, &sb.p_full[0], (uint32_t)i & 1u, &sb.abort, p.status))) break;
+        issue_pv(0, s, i == 0);
+        mma_commit_w(&sb.o_done[0]);
+      }
       const bool rp1 = mbar_test(&sb.p_full[1], (uint32_t)i & 1u);
       if (more) {
         if (!(ok = wait_ready(rk, &sb.k_full[s1], ph1, &sb.abort, p.status))) break;
-        issue_qk(0, s1);
-        mma_commit_w(&sb.s_full[0]);
+        if (more0) {
+          issue_qk(0, s1);
+          mma_commit_w(&sb.s_full[0]);
+        }
       }
       rv = more && mbar_test(&sb.v_full[s1], ph1);   // for the next tile
       // Query tile 1: P1 V, then the next S1.
@@ -363,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     uint32_t x[BN];
-    for (int i = 0; i < n_tiles; ++i) {
+    const int n_my = t ? n_tiles : n0;   // this query tile's key tiles
+    for (int i = 0; i < n_my; ++i) {
       if (!wait_warp(&sb.s_full[t], (uint32_t)i & 1u, &sb.abort, p.status)) {
         ok = false;
         break;
@@ -532,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sb.p_full[t]);
     }
     // ---- epilogue: O / l, special rows, LSE ----
-    if (ok && n_tiles > 0) ok = wait_warp(&sb.o_done[t], (uint32_t)(n_tiles - 1) & 1u, &sb.abort, p.status);
+    if (ok && n_my > 0) ok = wait_warp(&sb.o_done[t], (uint32_t)(n_my - 1) & 1u, &sb.abort, p.status);
     if (ok) {
       fence_after();
       const bool valid = qrow < p.Sq;
@@ -555,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          if (n_tiles > 0) {
+          if (n_my > 0) {
             tmem_ld32(o_tm + c * 32, o);
             tmem_ld_wait_regs<1>(o);
           }
@@ -571,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          if (n_tiles > 0) {
+          if (n_my > 0) {
             tmem_ld32(o_tm + c * 32, o);
             tmem_ld_wait_regs<1>(o);
           } else {
