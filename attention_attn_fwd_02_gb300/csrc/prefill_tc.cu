@@ -679,8 +679,13 @@ int prefill_tc_try(const Problem& p, const Split& sp, cudaStream_t st, int* used
   if (!tma_layout_ok(p.Q, p.q, p.Sq, p.H, p.B) || !tma_layout_ok(p.K, p.k, p.Sk, p.G, p.B) ||
       !tma_layout_ok(p.V, p.v, p.Sk, p.G, p.B) || !tma_layout_ok(p.O, p.o, p.Sq, p.H, p.B))
     return ATTN_OK;
-  const int rc = p.D == 256 ? prefill_tc1_launch(p, sp, st)
-                            : (p.D == 64 ? tc::launch_d<64>(p, sp, st) : tc::launch_d<128>(p, sp, st));
+  int rc = -1;
+  if (p.D == 256) {
+    rc = prefill_tc2_launch(p, sp, st);      // CTA pairs
+    if (rc < 0) rc = prefill_tc1_launch(p, sp, st);
+  } else {
+    rc = p.D == 64 ? tc::launch_d<64>(p, sp, st) : tc::launch_d<128>(p, sp, st);
+  }
   if (rc < 0) return ATTN_OK;  // tensor map refused: generic path
   *used = 1;
   return rc;

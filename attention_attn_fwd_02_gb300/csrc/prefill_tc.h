@@ -13,4 +13,9 @@ int prefill_tc_try(const Problem& p, const Split& s, cudaStream_t st, int* used)
 // The head_dim 256 kernel (one query tile per CTA, double-buffered S).
 // Returns -1 when TMA cannot describe the layout, else an ATTN_* status.
 int prefill_tc1_launch(const Problem& p, const Split& s, cudaStream_t st);
+
+// The head_dim 256 kernel on CTA pairs (cta_group::2): each pair shares its K
+// and V tiles.  Returns -1 when it does not apply (segment starts) or TMA
+// cannot describe the layout, else an ATTN_* status.
+int prefill_tc2_launch(const Problem& p, const Split& s, cudaStream_t st);
 }  // namespace attn

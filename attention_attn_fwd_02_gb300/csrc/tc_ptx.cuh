@@ -102,6 +102,86 @@ __device__ __forceinline__ bool wait_ready(bool ready, uint64_t* b, uint32_t par
   return wait_warp(b, parity, abort_flag, status);
 }
 
+// ---- CTA pairs (a 2-CTA cluster sharing tcgen05 work, cta_group::2) ----
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs: arrive, then wait for the whole cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive (release at cluster scope) on the barrier at the same offset in CTA `rank` of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* local_bar, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(su32(local_bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+// The same arrival without release semantics: it orders nothing by itself.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint64_t* local_bar, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(su32(local_bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+// Phase tests with acquire at cluster scope: for barriers that other CTAs
+// of the cluster (or their tensor cores) arrive on.
+__device__ __forceinline__ bool mbar_try_cl(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_cl(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait_bar_cl(uint64_t* b, uint32_t parity, int* abort_flag, int* status) {
+  if (mbar_try_cl(b, parity)) return true;
+  const uint64_t t0 = gtimer();
+  while (!mbar_try_cl(b, parity)) {
+    if (*(volatile int*)abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) {
+      *(volatile int*)abort_flag = 1;
+      atomicExch(status, ATTN_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ bool drain_bar_cl(uint64_t* b, uint32_t parity, int* status) {
+  const uint64_t t0 = gtimer();
+  while (!mbar_try_cl(b, parity)) {
+    if (gtimer() - t0 > kTimeoutNs) {
+      atomicExch(status, ATTN_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ bool wait_warp_cl(uint64_t* b, uint32_t parity, int* abort_flag, int* status) {
+  const bool ok = wait_bar_cl(b, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool wait_ready_cl(bool ready, uint64_t* b, uint32_t parity, int* abort_flag,
+                                              int* status) {
+  if (__all_sync(0xffffffffu, ready)) return true;
+  return wait_warp_cl(b, parity, abort_flag, status);
+}
+
 // Contiguous bulk copy global -> shared, completing on `bar` (both addresses
 // 16-byte aligned, `bytes` a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -170,6 +250,40 @@ __device__ __forceinline__ void mma_commit_w(uint64_t* b) {
       "{\n\t.reg .pred e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(b))
+      : "memory");
+}
+
+// Pair forms, issued by one elected lane of the leader CTA's warp: A rows
+// 0-127 come from the leader's operand and 128-255 from the follower's at the
+// same shared-memory (or TMEM) address, each CTA holds N/2 columns of B at the
+// same address, and each CTA's TMEM receives its own 128 rows of D.
+__device__ __forceinline__ void mma2_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_ts_w(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Completion of the pair MMAs issued so far arrives on the barrier at the
+// same offset in both CTAs.
+__device__ __forceinline__ void mma2_commit_both_w(uint64_t* b) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          su32(b)),
+      "h"((uint16_t)3)
       : "memory");
 }
 
