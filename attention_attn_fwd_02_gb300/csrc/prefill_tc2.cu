@@ -182,6 +182,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sb.mma_done, 1);
     for (int w = 0; w < 4; ++w) mbar_init(&sb.pair[w], 64);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // Q does not depend on the key plan: its copy starts at once (local
+    // barrier; the follower forwards its completion to the leader later).
+    mbar_expect_tx(&sb.q_full, C::kQTile);
+    for (int c = 0; c < D / 64; ++c) tma_load_4d(q_s + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0, h, b);
   }
   const int r = (warp % 4) * 32 + lane;  // softmax row = TMEM lane (warps 0-7)
   const int ch = warp / 4;                // key half / O half of a softmax thread
@@ -223,6 +227,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const bool any = hi_u > lo_u;
   const int j0 = any ? lo_u / BN : 0;
   const int n_span = any ? (hi_u + BN - 1) / BN - j0 : 0;   // key tiles spanning the union
+  // The first key tiles' halves start their way into L2 while the mask is
+  // scanned (their copies into the ring wait for the live-tile list).
+  if (warp == 8 && lane == 0) {
+    for (int t = 0; t < 2 && t < n_span; ++t) {
+      const int krow = (j0 + t) * BN;
+      for (int c = 0; c < 4; ++c) tma_prefetch_4d(&tm_k, c * 64, krow + (int)rank * kKHalf, g, b);
+      for (int c = 0; c < 2; ++c) tma_prefetch_4d(&tm_v, ((int)rank * 2 + c) * 64, krow, g, b);
+    }
+  }
   // A broadcast mask over a span of at most kMaskCap keys is copied to shared
   // memory once (every softmax thread reads it there), and key tiles whose
   // visible keys all have mask -inf are dropped from the CTA's work: their
@@ -296,8 +309,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 8) {
     // ---------------- TMA producer: this CTA's Q and halves ----------------
     if (lane == 0) {
-      mbar_expect_tx(&sb.q_full, C::kQTile);
-      for (int c = 0; c < D / 64; ++c) tma_load_4d(q_s + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0, h, b);
       UnitSeq seq{n_tiles};
       int kind, tile, issued = 0;
       while (seq.next(kind, tile)) {
