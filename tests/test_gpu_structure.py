@@ -42,6 +42,10 @@ TIMEOUT_CASES = {
                                         q_len=300, head_dim=64, causal=True),
     "prefill_d256": lambda: wl.make_case(name="to256", seed=73, dtype="f16", batch=1, heads=2, q_len=200,
                                          k_len=600, head_dim=256),
+    # segment starts route head_dim 256 to the single-CTA kernel
+    "prefill_d256_segments": lambda: wl.make_case(
+        name="to256s", seed=74, dtype="bf16", batch=1, heads=2, q_len=300, head_dim=256, causal=True,
+        causal_offset=0, seg=np.repeat(np.arange(0, 300, 100), 100).astype(np.int32)[None, :]),
     "decode_bf16": lambda: wl.decode_bnsh_bf16(seed=77, batch=2, capacity=1024, heads=8, kv_heads=2, min_len=600),
     "decode_int8": lambda: wl.make_case(name="to_q8", seed=78, dtype="bf16", batch=2, heads=8, kv_heads=2, q_len=1,
                                         k_len=2000, head_dim=128, k_lens=np.array([1500, 2000], dtype=np.int32),
