@@ -132,8 +132,9 @@ struct UnitSeq {
 template <int D, bool BF16, bool MASK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
-                       const int drop_first_copy, const int mask_stage, const Split sp) {
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       const Problem p, const int n_qblocks, const int drop_first_copy, const int mask_stage,
+                       const int o_tma, const Split sp) {
   using C = Cfg<D, MASK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -164,6 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    if (o_tma) prefetch_tmap(&tm_o);
     sb.live = 0u;
     sb.n_live = 0;
     sb.abort = 0;
@@ -199,16 +201,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lo = (int)lo64;
     hi = (int)(hi64 > lo64 ? hi64 : lo64);
   }
-  if (warp == 9) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&sb.tmem_base))
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-  }
-  fence_before();
-  __syncthreads();
-  // Both CTAs' barriers exist before either CTA arrives on the other's.
-  cluster_sync();
-  fence_after();
   // The pair's union of visible key ranges: both ends of a row's range are
   // non-decreasing in the row (no segment starts), so [lo of the pair's first
   // row, hi of its last row) covers it.  Both CTAs compute the same plan.
@@ -223,12 +215,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lo_u = (int)f_lo;
     hi_u = h64 > f_lo ? (int)h64 : -1;
   }
-  const uint32_t tmem = sb.tmem_base;
   const bool any = hi_u > lo_u;
   const int j0 = any ? lo_u / BN : 0;
   const int n_span = any ? (hi_u + BN - 1) / BN - j0 : 0;   // key tiles spanning the union
-  // The first key tiles' halves start their way into L2 while the mask is
-  // scanned (their copies into the ring wait for the live-tile list).
+  // The first key tiles' halves start their way into L2 while the pair
+  // starts up and the mask is scanned (their copies into the ring wait for
+  // the live-tile list).
   if (warp == 8 && lane == 0) {
     for (int t = 0; t < 2 && t < n_span; ++t) {
       const int krow = (j0 + t) * BN;
@@ -240,35 +232,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // memory once (every softmax thread reads it there), and key tiles whose
   // visible keys all have mask -inf are dropped from the CTA's work: their
   // probabilities are zero, so neither the maximum, the sum nor O sees them.
-  // NaN or +inf entries keep their tile (they make rows NaN).
+  // NaN or +inf entries keep their tile (they make rows NaN).  Every thread
+  // issues its loads (16-byte vectors when the row is aligned) before the
+  // pair's start-up barriers, so their latency overlaps them.
   const int mbase = j0 * BN;
   const bool staged = MASK && mask_stage && n_span > 0 && n_span <= kMaxListTiles;
-  if (staged) {
-    // Every thread issues all of its loads before using any (one memory round
-    // trip), stores the values and marks the tiles of its keys that are live.
-    const int mlen = min(p.Sk, (j0 + n_span) * BN) - mbase;
-    const float* src = p.M + p.m.off + (int64_t)b * p.m.bs + mbase;
-    uint32_t mine = 0u;
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-      constexpr int kVec = (kMaskCap / 4 + kThreads - 1) / kThreads;
-      float4 v[kVec];
+  const int mlen = staged ? min(p.Sk, (j0 + n_span) * BN) - mbase : 0;
+  const float* msrc = MASK ? p.M + p.m.off + (int64_t)b * p.m.bs + mbase : nullptr;
+  const bool mvec = staged && (reinterpret_cast<uintptr_t>(msrc) & 15) == 0;
+  constexpr int kVec = MASK ? (kMaskCap / 4 + kThreads - 1) / kThreads : 1;
+  float4 mv4[kVec];
+  if (mvec) {
 #pragma unroll
-      for (int j = 0; j < kVec; ++j) {
-        const int k = 4 * (threadIdx.x + j * kThreads);
-        v[j] = k + 3 < mlen ? __ldg(reinterpret_cast<const float4*>(src + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k < mlen && k + 3 >= mlen) {   // the ragged end
-          v[j].x = src[k];
-          v[j].y = k + 1 < mlen ? src[k + 1] : -INFINITY;
-          v[j].z = k + 2 < mlen ? src[k + 2] : -INFINITY;
-          v[j].w = -INFINITY;
-        }
+    for (int j = 0; j < kVec; ++j) {
+      const int k = 4 * (threadIdx.x + j * kThreads);
+      mv4[j] = k + 3 < mlen ? __ldg(reinterpret_cast<const float4*>(msrc + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k < mlen && k + 3 >= mlen) {   // the ragged end
+        mv4[j].x = msrc[k];
+        mv4[j].y = k + 1 < mlen ? msrc[k + 1] : -INFINITY;
+        mv4[j].z = k + 2 < mlen ? msrc[k + 2] : -INFINITY;
+        mv4[j].w = -INFINITY;
       }
+    }
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&sb.tmem_base))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  // Both CTAs' barriers exist before either CTA arrives on the other's (their
+  // initialisation was released to the cluster by its own fence, so the
+  // arrival is relaxed and does not wait for the mask loads in flight).
+  cluster_sync_relaxed();
+  fence_after();
+  const uint32_t tmem = sb.tmem_base;
+  if (staged) {
+    // Store the values and mark the tiles of this thread's keys that are live.
+    uint32_t mine = 0u;
+    if (mvec) {
 #pragma unroll
       for (int j = 0; j < kVec; ++j) {
         const int k = 4 * (threadIdx.x + j * kThreads);
         if (k >= mlen) continue;
-        reinterpret_cast<float4*>(m_s)[k / 4] = v[j];
-        const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        reinterpret_cast<float4*>(m_s)[k / 4] = mv4[j];
+        const float e[4] = {mv4[j].x, mv4[j].y, mv4[j].z, mv4[j].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int key = mbase + k + q;
@@ -281,7 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kSc; ++j) {
         const int k = threadIdx.x + j * kThreads;
-        v[j] = k < mlen ? src[k] : -INFINITY;
+        v[j] = k < mlen ? msrc[k] : -INFINITY;
       }
 #pragma unroll
       for (int j = 0; j < kSc; ++j) {
@@ -684,6 +693,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (valid && ch == 0)
           sp.part_lse[prow * sp.n_splits + split] = hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
       } else {
+        // With a tensor map for O, each warp stages its 32 rows x 128 channels
+        // in the ring, in the map's box layout (two boxes of 64 channels, rows
+        // of 128 bytes, 16-byte chunks swizzled by the row), and one lane
+        // stores them with two tiled copies: full 128-byte lines instead of
+        // 16 bytes of 32 rows per store instruction.  The ring is free here:
+        // no unit is copied after the last one, and the last P V (which
+        // read it) has completed.  Rows past the end of Q are not written.
+        const int wr0 = (warp % 4) * 32;   // the warp's first row in the CTA
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           uint32_t o[32];
@@ -701,11 +718,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const float bb = hidden_row ? fill : __uint_as_float(o[e + 1]) * inv;
             w[e / 2] = pack2<BF16>(a, bb);
           }
-          if (valid) {
+          if (o_tma) {
+            uint8_t* rowp = ring + (ch * 2 + c / 2) * (BM * 128) + r * 128;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              *reinterpret_cast<uint4*>(rowp + ((((c % 2) * 4 + v4) ^ (r & 7)) * 16)) =
+                  make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          } else if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
           }
+        }
+        if (o_tma) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0 && q0 + wr0 < p.Sq) {
+            for (int cc = 0; cc < 2; ++cc)
+              tma_store_4d(&tm_o, ring + (ch * 2 + cc) * (BM * 128) + wr0 * 128, (ch * 2 + cc) * 64, q0 + wr0, h, b);
+            bulk_store_commit_wait_read();
+          }
+          __syncwarp();
         }
         if (valid && p.lse && ch == 0)
           p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
@@ -726,11 +759,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int D, bool BF16, bool MASK>
 int launch(const Problem& p, const Split& sp, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!tma_map_bhsd(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q, BM) ||
       !tma_map_bhsd(&mk, p.K, p.dtype, D, p.Sk, p.G, p.B, p.k, kKHalf) ||
       !tma_map_bhsd(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v, BN))
     return -1;  // not describable: caller falls back
+  // O is stored by tiled copies of 32 rows when TMA can describe it (the
+  // final output only: key-range partials are float32 rows of their own).
+  const int o_tma = sp.n_splits == 1 && tma_map_bhsd(&mo, p.O, p.dtype, D, p.Sq, p.H, p.B, p.o, 32) ? 1 : 0;
+  if (!o_tma) memset(&mo, 0, sizeof mo);
   const int npq = (p.Sq + 2 * BM - 1) / (2 * BM);   // pairs per (batch, head)
   const int64_t blocks = 2 * (int64_t)npq * p.H * p.B * sp.n_splits;
   if (blocks > 0x7fffffff) return -1;
@@ -740,7 +777,7 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
   const int mask_stage = (MASK && p.m.hs == 0 && p.m.rs == 0) ? 1 : 0;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, npq, drop, mask_stage, sp);
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, mo, p, npq, drop, mask_stage, o_tma, sp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
