@@ -379,6 +379,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t x[BN];
     const int n_my = t ? n_tiles : n0;   // this query tile's key tiles
+    // A mask with a row per query (not staged): all 128 values of the tile
+    // are loaded into x at once (one memory round trip a tile, not one per
+    // few keys), and S is then added to them 32 columns at a time.  Mask
+    // values of hidden keys inside the key axis are read and then replaced by
+    // -inf with the rest of the hidden scores.  (Issuing these loads before
+    // the wait for S keeps x live across it, and the compiler then spills.)
+    const bool mask_pf = MASK && mask_nat && !mask_bcast;
+    auto load_mask = [&](int i) {
+      const int k0 = (j0 + i) * BN;
+      const float* mp = mrow ? mrow + k0 : nullptr;
+      if (mp && k0 + BN <= p.Sk && ((uintptr_t)mp & 15) == 0) {
+#pragma unroll
+        for (int j = 0; j < BN / 4; ++j) {
+          const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
+          x[4 * j] = __float_as_uint(v4.x);
+          x[4 * j + 1] = __float_as_uint(v4.y);
+          x[4 * j + 2] = __float_as_uint(v4.z);
+          x[4 * j + 3] = __float_as_uint(v4.w);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) x[e] = __float_as_uint((mp && k0 + e < p.Sk) ? mp[e] : 0.f);
+      }
+    };
     for (int i = 0; i < n_my; ++i) {
       if (!wait_warp(&sb.s_full[t], (uint32_t)i & 1u, &sb.abort, p.status)) {
         ok = false;
@@ -406,40 +430,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       float corr = 1.f;
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
-        if (mask_nat) {
+        if (mask_pf) {
+          load_mask(i);
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t sv[32];
+            tmem_ld32(s_tm + c * 32, sv);
+            tmem_ld_wait_regs<1>(sv);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int xe = c * 32 + e;
+              float v0, v1;
+              fma2(v0, v1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), scale2,
+                   f2u(__uint_as_float(x[xe]), __uint_as_float(x[xe + 1])));
+              x[xe] = __float_as_uint(v0);
+              x[xe + 1] = __float_as_uint(v1);
+            }
+          }
+          if (!(k0 >= lo && k0 + BN <= hi)) {
+#pragma unroll
+            for (int e = 0; e < BN; ++e) {
+              const int kk = k0 + e;
+              if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
+            }
+          }
+        } else if (mask_nat) {
+          // Staged broadcast mask (out-of-range keys are hidden below).
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) {
             tmem_ld32(s_tm + c * 32, x + c * 32);
             tmem_ld_wait_regs<1>(x + c * 32);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {   // 16 keys at a time keeps few mask values live
-              float mv[16];
-              const int kc = k0 + c * 32 + hf * 16;
-              const float* mp = mrow ? mrow + kc : nullptr;
-              if (mask_bcast) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) mv[e] = ms[c * 32 + hf * 16 + e];   // out-of-range keys are hidden below
-              } else if (mp && kc >= lo && kc + 16 <= hi && ((uintptr_t)mp & 15) == 0) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const float4 v4 = __ldg(reinterpret_cast<const float4*>(mp) + j);
-                  mv[4 * j] = v4.x;
-                  mv[4 * j + 1] = v4.y;
-                  mv[4 * j + 2] = v4.z;
-                  mv[4 * j + 3] = v4.w;
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) mv[e] = (mp && kc + e >= lo && kc + e < hi) ? mp[e] : 0.f;
-              }
-#pragma unroll
-              for (int e = 0; e < 16; e += 2) {
-                const int xe = c * 32 + hf * 16 + e;
-                float v0, v1;
-                fma2(v0, v1, __uint_as_float(x[xe]), __uint_as_float(x[xe + 1]), scale2, f2u(mv[e], mv[e + 1]));
-                x[xe] = __float_as_uint(v0);
-                x[xe + 1] = __float_as_uint(v1);
-              }
+            for (int e = 0; e < 32; e += 2) {
+              const int xe = c * 32 + e;
+              float v0, v1;
+              fma2(v0, v1, __uint_as_float(x[xe]), __uint_as_float(x[xe + 1]), scale2, f2u(ms[xe], ms[xe + 1]));
+              x[xe] = __float_as_uint(v0);
+              x[xe + 1] = __float_as_uint(v1);
             }
           }
           if (!(k0 >= lo && k0 + BN <= hi)) {

@@ -275,6 +275,18 @@ def masked_gqa_bf16(seed: int = 3, batch: int = 2, seq: int = 4096, heads: int =
                      causal=False, causal_offset=None, value_scale=0.5, mask=mask, mask_kind="b11k")
 
 
+def rowmask_gqa_bf16(seed: int = 7, batch: int = 2, seq: int = 4096, heads: int = 32, kv_heads: int = 8) -> Case:
+    """The long GQA prefill's shapes with a float32 mask of one row per query, shared by every batch entry
+    and head ([1,1,Q,K], 64 MiB): N(0,1) values, the last key_len/8 keys -inf (a context measurement of the
+    per-row mask path)."""
+    r = rng(seed, MASK_ID)
+    mask = r.standard_normal((1, 1, seq, seq)).astype(np.float32)
+    mask[:, :, :, seq - seq // 8:] = -np.inf
+    return make_case(name=f"rowmask_gqa_bf16_b{batch}_h{heads}_kv{kv_heads}_s{seq}_d128", seed=seed, dtype="bf16",
+                     layout="bhsd", batch=batch, heads=heads, kv_heads=kv_heads, q_len=seq, head_dim=128,
+                     causal=False, causal_offset=None, value_scale=0.5, mask=mask, mask_kind="11qk")
+
+
 def short_query_cross_bf16(seed: int = 6, batch: int = 1, heads: int = 32, kv_heads: int = 8, q_len: int = 64,
                            k_len: int = 8192) -> Case:
     """A few queries against a long key axis (bf16, head dim 128, head-first, non-causal): too few blocks

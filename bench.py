@@ -559,6 +559,7 @@ CASES = {
     "long_causal_gqa_bf16": lambda: wl.long_causal_gqa_bf16(),
     "dense_gqa_bf16": lambda: wl.dense_gqa_bf16(),
     "masked_gqa_bf16": lambda: wl.masked_gqa_bf16(),
+    "rowmask_gqa_bf16": lambda: wl.rowmask_gqa_bf16(),
     "short_query_cross_bf16": lambda: wl.short_query_cross_bf16(),
     "decode_bnsh_bf16": lambda: wl.decode_bnsh_bf16(),
     "decode_bnsh_int8": lambda: wl.decode_bnsh_int8(),
@@ -635,7 +636,7 @@ def run_case(args):
 # causal GQA with documents, the head_dim-256 masked cross-attention in both
 # MaskedRows modes, and the context cases.
 EXTRA_CASES = ("tiny_f32_mha", "gqa_doc_causal_bf16", "cross_mask_f16", "cross_mask_f16_zero", "dense_gqa_bf16",
-               "masked_gqa_bf16", "short_query_cross_bf16", "decode_bnsh_int8")
+               "masked_gqa_bf16", "rowmask_gqa_bf16", "short_query_cross_bf16", "decode_bnsh_int8")
 
 
 def extra_cases(pk, pk_kind):

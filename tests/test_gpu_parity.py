@@ -93,6 +93,13 @@ EDGE = [
     # head_dim 256 with two and three key tiles: the last P V may still be two phases behind
     ("bf16", "bhsd", 2, 4, 2, 200, 100, 256, False, None, False, False, None, "nan", False),
     ("f16", "bshd", 1, 3, 1, 260, 190, 256, True, None, False, True, None, "zero", False),
+    # masks with a row per query on the tensor-core kernels: rows of 517 floats (not 16-byte aligned,
+    # element loads) with a ragged last key tile; aligned rows (vector loads) with segments, and with a
+    # ragged last tile; head_dim 256 on CTA pairs
+    ("bf16", "bhsd", 2, 4, 2, 300, 517, 128, True, None, False, True, "11qk", "nan", False),
+    ("f16", "bshd", 1, 4, 1, 257, 640, 64, False, None, True, False, "bhqk", "zero", False),
+    ("bf16", "bhsd", 1, 2, 2, 200, 1000, 128, False, None, False, False, "bhqk", "zero", False),
+    ("bf16", "bshd", 1, 2, 1, 260, 300, 256, True, None, False, True, "bhqk", "nan", False),
 ]
 
 
@@ -494,14 +501,16 @@ def test_ex2_probe_runs_and_keeps_its_chains_bounded():
     assert np.all(np.isfinite(s)) and np.all(s >= -2048.0) and np.all(s <= -1024.0)
 
 
+@pytest.mark.parametrize("per_row", [False, True])
 @pytest.mark.parametrize("D,dtype,causal", [(128, "bf16", False), (128, "f16", True), (64, "bf16", True),
                                              (256, "f16", False), (256, "bf16", True)])
-def test_scores_rising_far_above_the_reference_maximum(D, dtype, causal):
+def test_scores_rising_far_above_the_reference_maximum(D, dtype, causal, per_row):
     """Scores that jump well above a row's reference maximum after its first
     key tiles: by 43 log2 units (P up to 2^43 in bf16 kept without a rescale; in
     f16, past 2^15, the tile is redone), by 87
     and 88 (the tile is redone with its maximum), and to +inf at one key (a
-    NaN row).  All against the oracle."""
+    NaN row).  All against the oracle; the same values also as a mask with a
+    row per query ([B,H,Q,K], read from global memory, reloaded on a redo)."""
     B, H, Sq, Sk = 3, 4, 256, 640
     r = np.random.default_rng(77 + D)
     mask = (r.standard_normal((B, 1, 1, Sk)) * 0.5).astype(np.float32)
@@ -510,8 +519,12 @@ def test_scores_rising_far_above_the_reference_maximum(D, dtype, causal):
     mask[1, 0, 0, 500:] += 1.0
     mask[2, 0, 0, 150:] += 20.0
     mask[2, 0, 0, 400] = np.inf
+    kind = "b11k"
+    if per_row:
+        mask = np.ascontiguousarray(np.broadcast_to(mask, (B, H, Sq, Sk)))
+        kind = "bhqk"
     c = wl.make_case(name=f"rise{D}", seed=88, dtype=dtype, batch=B, heads=H, q_len=Sq, k_len=Sk, head_dim=D,
-                     causal=causal, causal_offset=Sk - Sq if causal else None, mask=mask)
+                     causal=causal, causal_offset=Sk - Sq if causal else None, mask=mask, mask_kind=kind)
     st, _ = run_and_compare(c)
     assert st["nan_rows"] == H * (Sq if not causal else Sq - (400 - (Sk - Sq)))
 
