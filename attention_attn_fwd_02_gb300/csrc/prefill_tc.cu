@@ -81,6 +81,22 @@ struct Cfg {
   static_assert(2 * BN + 2 * D <= 512, "TMEM budget");
 };
 
+// Scores of a tile's keys e outside [a, z) (key offsets within the tile)
+// become -inf.  Most tiles that need it are cut at one end only (the causal
+// diagonal, a key length), which takes one comparison an element.
+template <int N>
+__device__ __forceinline__ void hide_outside(uint32_t* x, int a, int z) {
+  if (a <= 0) {
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if (e >= z) x[e] = __float_as_uint(-INFINITY);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if (e < a || e >= z) x[e] = __float_as_uint(-INFINITY);
+  }
+}
+
 template <int D, bool BF16, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -114,6 +130,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = hb % p.H, b = hb / p.H;
   const int g = h / p.qpg;
   const int q0 = qb * 2 * BM;
+  // Without a window or segment starts every row's keys start at the key
+  // range's start (kr0, a multiple of BN), so the CTA's first K and V tiles
+  // are known before any key length is read from global memory: their copies
+  // start at once, with Q's, into stage 0.  (Not with the test hook, which
+  // drops the producer's first K copy.)
+  const bool early = !(p.causal && p.window >= 0) && p.seg == nullptr && !(drop_first_copy && blockIdx.x == 0);
 
   if (threadIdx.x == 0) {
     // The copies' descriptors start on their way before anything else.
@@ -142,6 +164,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tt = 0; tt < 2; ++tt)
       for (int c = 0; c < C::kChunks; ++c)
         tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
+    if (early) {
+      const int krow = (int)kr0;
+      mbar_expect_tx(&sb.k_full[0], C::kKTile);
+      for (int c = 0; c < C::kChunks; ++c) tma_load_4d(k_s + c * BN * 128, &tm_k, &sb.k_full[0], c * 64, krow, g, b);
+      const uint32_t mbytes = MASK && mask_bcast ? (uint32_t)min(BN, p.Sk - krow) * 4u : 0u;
+      mbar_expect_tx(&sb.v_full[0], C::kKTile + mbytes);
+      if (mbytes) bulk_load(m_s, p.M + p.m.off + (int64_t)b * p.m.bs + krow, mbytes, &sb.v_full[0]);
+      for (int c = 0; c < C::kChunks; ++c) tma_load_4d(v_s + c * BN * 128, &tm_v, &sb.v_full[0], c * 64, krow, g, b);
+    }
   }
   // ---- row ranges and their union ----
   const int t = warp / 4;                       // query tile of a softmax thread
@@ -209,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int issued = 0;          // tiles whose K and V copies were both issued
-      int k_only = -1;         // a tile whose K copy was issued but not its V copy
-      for (int i = 0; i < n_tiles; ++i) {
+      int issued = early ? 1 : 0;   // tiles whose K and V copies were both issued
+      int k_only = -1;              // a tile whose K copy was issued but not its V copy
+      for (int i = issued; i < n_tiles; ++i) {
         const int s = i % C::kStages;
         const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
         const int krow = (j0 + i) * BN;
@@ -500,13 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tm + c * 32, x + c * 32);
           tmem_ld_wait_regs<BN / 32>(x);
-          if (!(k0 >= lo && k0 + BN <= hi)) {
-#pragma unroll
-            for (int e = 0; e < BN; ++e) {
-              const int kk = k0 + e;
-              if (kk < lo || kk >= hi) x[e] = __float_as_uint(-INFINITY);
-            }
-          }
+          if (!(k0 >= lo && k0 + BN <= hi)) hide_outside<BN>(x, lo - k0, hi - k0);
         }
         if (scan) {
           float mx0 = -INFINITY, mx1 = -INFINITY;

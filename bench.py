@@ -568,9 +568,11 @@ CASES = {
 }
 
 
-def time_case(case, steps: int, warmup: int, flush: bool = True):
+def time_case(case, steps: int, warmup: int, flush: bool = True, flush_kind: str = "write"):
     """Median and minimum device time (ms) of one call of `case` through the C ABI,
-    inputs resident in HBM, an L2 flush (256 MiB write) before each timed call."""
+    inputs resident in HBM, an L2 flush before each timed call: a 256 MiB write
+    (which leaves L2 full of dirty lines, written back during the call), or with
+    flush_kind "read" a 256 MiB read (L2 left clean and holding no input)."""
     import torch
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from gpu_util import GpuCase
@@ -583,7 +585,10 @@ def time_case(case, steps: int, warmup: int, flush: bool = True):
     ms = []
     for _ in range(steps):
         if fl is not None:
-            fl.zero_()
+            if flush_kind == "read":
+                fl.sum(dtype=torch.int64)
+            else:
+                fl.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
         g.run()
@@ -648,6 +653,12 @@ def extra_cases(pk, pk_kind):
         med, mn = time_case(case, 50 if small else 10, 5 if small else 3)
         d = {"workload": case.name, "ms_median": med, "ms_min": mn}
         d.update(case_line(case, med, pk, pk_kind))
+        if case.decode:
+            # A decode reads more than L2 holds; beside the write-flushed figure,
+            # the same call after a 256 MiB read (no dirty lines to write back).
+            med_r, _ = time_case(case, 10, 3, flush_kind="read")
+            r = case_line(case, med_r, pk, pk_kind)
+            d["after_read_flush"] = {"ms_median": med_r, "value": r["value"], "frac": r["frac"]}
         d["status"] = attn.status_string(attn.attn_device_status())
         out[name] = d
     return out
