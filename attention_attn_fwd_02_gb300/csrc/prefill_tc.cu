@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < BN; ++e) x[e] = __float_as_uint((mp && k0 + e < p.Sk) ? mp[e] : 0.f);
+        for (int e = 0; e < BN; ++e) x[e] = __float_as_uint((mp && k0 + e < p.Sk) ? __ldg(mp + e) : 0.f);
       }
     };
     for (int i = 0; i < n_my; ++i) {
