@@ -97,7 +97,7 @@ __device__ __forceinline__ void hide_outside(uint32_t* x, int a, int z) {
   }
 }
 
-template <int D, bool BF16, bool MASK>
+template <int D, bool BF16, bool MASK, bool XF>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
@@ -395,12 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Soft-capping: the scaled product s becomes cap2 * tanh(s_raw * kinv) in log2 units.
     const bool capped = p.softcap > 0.f;
     const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
-    // With a mask, no softcap and a positive scale the scores stay in natural
-    // units, s * scale + mask (one packed FMA for two keys, the mask read as
-    // float4 where it can be), and the exponent's multiplier takes log2(e);
-    // other transformed scores are formed in log2 units.
+    // Without softcap and with a positive scale the scores of a masked problem
+    // stay in natural units, s * scale + mask (one packed FMA for two keys),
+    // and the exponent's multiplier takes log2(e).  Scores under a softcap or a
+    // scale that is not positive are formed in log2 units one at a time, in an
+    // instantiation of their own (XF, chosen by the launcher from the same
+    // test), so that the common kernels do not carry that path's registers.
     const bool mask_nat = MASK && !capped && sc > 0.f;
-    const bool explicit_x = (MASK && !mask_nat) || !(sc > 0.f) || capped;
+    const bool explicit_x = XF;
     const float c_eff = mask_nat ? kLog2e : (explicit_x ? 1.f : sc);
     const uint64_t scale2 = f2u(p.scale, p.scale);
     const float* mrow = nullptr;
@@ -676,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -----------------------------------------------------------------------
 
-template <int D, bool BF16, bool MASK>
+template <int D, bool BF16, bool MASK, bool XF>
 int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!tma_map_bhsd(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q, BM) ||
@@ -687,12 +689,12 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   const int64_t blocks = (int64_t)nqb * p.H * p.B * sp.n_splits;
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D>::kSmem + 1024;
-  auto kern = prefill_tc_kernel<D, BF16, MASK>;
+  auto kern = prefill_tc_kernel<D, BF16, MASK, XF>;
   // setmaxnreg.inc waits until the block's register pool holds the larger
   // count, so the pool the kernel is launched with must cover the split.
   static const bool regs_ok = [] {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, (const void*)prefill_tc_kernel<D, BF16, MASK>) != cudaSuccess) return false;
+    if (cudaFuncGetAttributes(&a, (const void*)prefill_tc_kernel<D, BF16, MASK, XF>) != cudaSuccess) return false;
     return a.numRegs * kThreads >= kSplitRegs;
   }();
   if (!regs_ok) return -1;
@@ -710,11 +712,17 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+template <int D, bool XF>
+int launch_x(const Problem& p, const Split& sp, cudaStream_t st) {
+  const bool m = p.M != nullptr;
+  if (p.dtype == ATTN_BF16) return m ? launch<D, true, true, XF>(p, sp, st) : launch<D, true, false, XF>(p, sp, st);
+  return m ? launch<D, false, true, XF>(p, sp, st) : launch<D, false, false, XF>(p, sp, st);
+}
+
 template <int D>
 int launch_d(const Problem& p, const Split& sp, cudaStream_t st) {
-  const bool m = p.M != nullptr;
-  if (p.dtype == ATTN_BF16) return m ? launch<D, true, true>(p, sp, st) : launch<D, true, false>(p, sp, st);
-  return m ? launch<D, false, true>(p, sp, st) : launch<D, false, false>(p, sp, st);
+  const bool xf = p.softcap > 0.f || !(p.scale * kLog2e > 0.f);
+  return xf ? launch_x<D, true>(p, sp, st) : launch_x<D, false>(p, sp, st);
 }
 
 }  // namespace tc
