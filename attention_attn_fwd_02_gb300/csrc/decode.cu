@@ -170,7 +170,9 @@ __device__ __forceinline__ uint32_t sw_off(int row, int d) {
   return (uint32_t)((d >> 6) * (kMStageKeys * 128) + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4));
 }
 
-template <bool BF16>
+// XF: scores under a softcap or an additive mask (an instantiation of its
+// own, so that the plain kernel carries neither path).
+template <bool BF16, bool XF>
 __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                               const __grid_constant__ CUtensorMap tm_v,
                                                               const Problem p, const Split sp, const int n_hc,
@@ -265,9 +267,9 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const __grid_const
     }
   }
   const float c = p.scale * kLog2e;
-  const bool capped = p.softcap > 0.f;
+  const bool capped = XF && p.softcap > 0.f;
   const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
-  const float* mrow = p.M ? p.M + p.m.off + (int64_t)b * p.m.bs : nullptr;
+  const float* mrow = XF && p.M ? p.M + p.m.off + (int64_t)b * p.m.bs : nullptr;
 
   float o[16][4];
 #pragma unroll
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const __grid_const
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool XF>
 int launch_mma(const Problem& p, const Split& s, cudaStream_t st) {
   CUtensorMap mk, mv;
   if (!tma_map_bhsd(&mk, p.K, p.dtype, kD, p.Sk, p.G, p.B, p.k, kMStageKeys) ||
@@ -440,7 +442,7 @@ int launch_mma(const Problem& p, const Split& s, cudaStream_t st) {
   const int64_t blocks = (int64_t)s.n_splits * n_hc * p.G * p.B;
   if (blocks <= 0 || blocks > 0x7fffffff) return -1;
   const int smem = kMStages * 2 * kMTile + 1024;
-  auto kern = decode_mma_kernel<BF16>;
+  auto kern = decode_mma_kernel<BF16, XF>;
   if (ensure_smem((const void*)kern, smem) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
@@ -459,7 +461,9 @@ int decode_fast_try(const Problem& p, const Split& s, cudaStream_t st, int* used
   if (p.kv_int8) return ATTN_OK;
   if (p.D != dec::kD || p.Sq != 1 || s.n_splits < 1) return ATTN_OK;
   if (!tma_layout_ok(p.K, p.k, p.Sk, p.G, p.B) || !tma_layout_ok(p.V, p.v, p.Sk, p.G, p.B)) return ATTN_OK;
-  const int rc = p.dtype == ATTN_BF16 ? dec::launch_mma<true>(p, s, st) : dec::launch_mma<false>(p, s, st);
+  const bool xf = p.softcap > 0.f || p.M != nullptr;
+  const int rc = p.dtype == ATTN_BF16 ? (xf ? dec::launch_mma<true, true>(p, s, st) : dec::launch_mma<true, false>(p, s, st))
+                                      : (xf ? dec::launch_mma<false, true>(p, s, st) : dec::launch_mma<false, false>(p, s, st));
   if (rc < 0) return ATTN_OK;
   *used = 1;
   return rc;

@@ -105,7 +105,9 @@ __device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
-template <bool BF16, int NT>
+// XF: scores under a softcap or an additive mask (an instantiation of its
+// own, so that the plain kernel carries neither path).
+template <bool BF16, int NT, bool XF>
 __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v,
                                                              const Problem p, const Split sp, const int n_hc,
@@ -217,10 +219,10 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
       kinit[j][1] = -kBias * q1;
     }
   }
-  const bool capped = p.softcap > 0.f;
+  const bool capped = XF && p.softcap > 0.f;
   const float kinv = capped ? 1.f / (p.softcap * kLog2e) : 0.f, cap2 = p.softcap * kLog2e;
-  const float* mrow = p.M ? p.M + p.m.off + (int64_t)b * p.m.bs : nullptr;
-  const bool plain = !capped && !mrow;
+  const float* mrow = XF && p.M ? p.M + p.m.off + (int64_t)b * p.m.bs : nullptr;
+  const bool plain = !XF;
 
   // O^T accumulators: o[c][j] rows = channels 16c + 2gid (rows gid) and
   // 16c + 2gid + 1 (rows gid + 8), columns = heads 8j + 2tig, + 1.  ls[j]
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreads) decode_q8_kernel(const __grid_consta
   }
 }
 
-template <bool BF16, int NT>
+template <bool BF16, int NT, bool XF>
 int launch(const Problem& p, const Split& s, cudaStream_t st) {
   CUtensorMap mk, mv;
   if (!tma_map_bhsd_u8(&mk, p.K, kD, p.Sk, p.G, p.B, p.k, kStageKeys) ||
@@ -417,16 +419,22 @@ int launch(const Problem& p, const Split& s, cudaStream_t st) {
   const int64_t blocks = (int64_t)s.n_splits * n_hc * p.G * p.B;
   if (blocks <= 0 || blocks > 0x7fffffff) return -1;
   const int smem = kStages * 2 * kTile + 1024;
-  auto kern = decode_q8_kernel<BF16, NT>;
+  auto kern = decode_q8_kernel<BF16, NT, XF>;
   if (ensure_smem((const void*)kern, smem) != cudaSuccess) return ATTN_ERR_CUDA;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
   kern<<<(unsigned)blocks, kThreads, smem, st>>>(mk, mv, p, s, n_hc, drop);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+template <bool BF16, bool XF>
+int launch_x(const Problem& p, const Split& s, cudaStream_t st) {
+  return p.qpg <= 8 ? launch<BF16, 1, XF>(p, s, st) : launch<BF16, 2, XF>(p, s, st);
+}
+
 template <bool BF16>
 int launch(const Problem& p, const Split& s, cudaStream_t st) {
-  return p.qpg <= 8 ? launch<BF16, 1>(p, s, st) : launch<BF16, 2>(p, s, st);
+  const bool xf = p.softcap > 0.f || p.M != nullptr;
+  return xf ? launch_x<BF16, true>(p, s, st) : launch_x<BF16, false>(p, s, st);
 }
 
 }  // namespace dq8

@@ -131,7 +131,7 @@ struct UnitSeq {
   }
 };
 
-template <int D, bool BF16, bool MASK>
+template <int D, bool BF16, bool MASK, bool XF>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
@@ -439,9 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float kinv = capped ? p.scale / p.softcap : 0.f, cap2 = p.softcap * kLog2e;
     // With a mask, no softcap and a positive scale the scores stay in natural
     // units, s * scale + mask (one packed FMA for two keys), and the exponent's
-    // multiplier takes log2(e); other transformed scores are formed in log2 units.
+    // multiplier takes log2(e); scores under a softcap or a scale that is not
+    // positive are formed in log2 units, in an instantiation of their own (XF,
+    // chosen by the launcher from the same test).
     const bool mask_nat = MASK && !capped && sc > 0.f;
-    const bool explicit_x = (MASK && !mask_nat) || !(sc > 0.f) || capped;
+    const bool explicit_x = XF;
     const float c_eff = mask_nat ? kLog2e : (explicit_x ? 1.f : sc);
     const uint64_t scale2 = f2u(p.scale, p.scale);
     const float* mrow = nullptr;
@@ -678,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool MASK>
+template <int D, bool BF16, bool MASK, bool XF>
 int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!tma_map_bhsd(&mq, p.Q, p.dtype, D, p.Sq, p.H, p.B, p.q, BM) ||
@@ -689,7 +691,7 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   const int64_t blocks = (int64_t)nqb * p.H * p.B * sp.n_splits;
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D, MASK>::kSmem + 1024;
-  auto kern = prefill_tc1_kernel<D, BF16, MASK>;
+  auto kern = prefill_tc1_kernel<D, BF16, MASK, XF>;
   cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
@@ -701,12 +703,20 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
 
 }  // namespace tc1
 
-int prefill_tc1_launch(const Problem& p, const Split& sp, cudaStream_t st) {
+namespace tc1 {
+template <bool XF>
+int launch_x(const Problem& p, const Split& sp, cudaStream_t st) {
   const bool m = p.M != nullptr;
-  if (p.D != 256) return -1;
   if (p.dtype == ATTN_BF16)
-    return m ? tc1::launch<256, true, true>(p, sp, st) : tc1::launch<256, true, false>(p, sp, st);
-  return m ? tc1::launch<256, false, true>(p, sp, st) : tc1::launch<256, false, false>(p, sp, st);
+    return m ? launch<256, true, true, XF>(p, sp, st) : launch<256, true, false, XF>(p, sp, st);
+  return m ? launch<256, false, true, XF>(p, sp, st) : launch<256, false, false, XF>(p, sp, st);
+}
+}  // namespace tc1
+
+int prefill_tc1_launch(const Problem& p, const Split& sp, cudaStream_t st) {
+  if (p.D != 256) return -1;
+  const bool xf = p.softcap > 0.f || !(p.scale * tc1::kLog2e > 0.f);
+  return xf ? tc1::launch_x<true>(p, sp, st) : tc1::launch_x<false>(p, sp, st);
 }
 
 }  // namespace attn
