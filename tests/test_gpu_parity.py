@@ -352,6 +352,7 @@ TRANSFORMS = [
     ("f16", "bshd", 2, 4, 2, 150, 400, 256, -60, 0.0, "smooth", "b11k"),     # head_dim 256, smooth softmax,
                                                                              # first rows see no key
     ("f16", "bshd", 1, 4, 4, 129, 300, 256, None, 1.5, "heads", None),       # head_dim 256, cap + sink
+    ("bf16", "bshd", 2, 4, 2, 260, 300, 256, None, 2.0, "none", "b11k"),     # head_dim 256 pairs, cap + mask
     ("f32", "bshd", 2, 2, 1, 70, 90, 32, 3, 2.0, "heads", "bhqk"),           # CUDA-core float32
     ("f16", "bhsd", 1, 4, 2, 129, 129, 96, 0, 0.0, "heads", None),           # CUDA-core half path
 ]
@@ -379,6 +380,32 @@ def test_softcap_and_sink(i):
     assert st["nan_rows"] == 0      # with a sink a row without keys gives O = 0, not NaN
 
 
+NEG_SCALE = [
+    # head_dim, mask, segment starts: the transformed-score instantiations of the
+    # tensor-core kernels without a softcap (a scale that is not positive)
+    (64, False, False),
+    (128, True, False),
+    (256, True, False),
+    (256, False, True),     # segment starts: the single-CTA head_dim-256 kernel
+]
+
+
+@pytest.mark.parametrize("i", range(len(NEG_SCALE)))
+def test_negative_scale_takes_the_transform_path(i):
+    D, masked, segs = NEG_SCALE[i]
+    B, H, G, Sq, Sk = 2, 4, 2, 200, 260
+    r = np.random.default_rng(1300 + i)
+    mask = None
+    if masked:
+        mask = r.standard_normal((B, 1, 1, Sk)).astype(np.float32)
+        mask[r.random(mask.shape) < 0.1] = -np.inf
+    seg = np.repeat(np.arange(0, Sq, 50), 50).astype(np.int32)[None, :].repeat(B, 0) if segs else None
+    c = wl.make_case(name=f"neg{i}", seed=1350 + i, dtype="bf16", layout="bhsd", batch=B, heads=H, kv_heads=G,
+                     q_len=Sq, k_len=Sk, head_dim=D, scale=-0.05, causal=True, causal_offset=Sk - Sq, mask=mask,
+                     seg=seg)
+    run_and_compare(c)
+
+
 DECODE_TF = [
     # dtype, layout, B, H, G, Sq, Sk (capacity), D, offset, softcap, sink, mask
     ("bf16", "bshd", 3, 16, 4, 1, 2000, 128, None, 1.5, "heads", "b11k"),   # tensor-core split pass
@@ -390,6 +417,31 @@ DECODE_TF = [
 @pytest.mark.parametrize("i", range(len(DECODE_TF)))
 def test_decode_softcap_and_sink(i):
     run_and_compare(transform_case(100 + i, DECODE_TF[i], decode=True))
+
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_decode_result_does_not_depend_on_what_the_workspace_held(int8):
+    """Every partial the merge reads is written by the same call: a workspace
+    full of 0xFF bytes (NaN floats), the same workspace reused by the next
+    call, and one full of zeros all give the oracle's result, with key
+    lengths of 0 and 1 among the rows."""
+    torch = torch_mod()
+    kw = dict(kv_dtype="i8") if int8 else {}
+    c = wl.make_case(name="wsre", seed=1401, dtype="bf16", batch=5, heads=16, kv_heads=4, q_len=1, k_len=3000,
+                     head_dim=128, k_lens=np.array([3000, 1, 0, 1777, 2999], dtype=np.int32), decode=True, **kw)
+    ref_o, ref_l = oracle_full(c)
+    g = GpuCase(c, lse=True)
+    need = attn.attn_decode_workspace_size(g.prob)
+    g.ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    g.ws_bytes = need
+    for fill in (None, None, 0):
+        if fill is not None:
+            g.ws.fill_(fill)
+        g.run()
+        o, l, _ = g.outputs()
+        g.check_guards()
+        compare(o, l, ref_o, ref_l, "bf16", "nan", c.name)
+        assert attn.attn_device_status() == attn.ATTN_OK
 
 
 def test_decode_single_range_generic_pass():
