@@ -323,6 +323,11 @@ SPLIT = {
         name="splitks", seed=2204, dtype="bf16", layout="bhsd", batch=3, heads=4, kv_heads=1, q_len=200, k_len=3000,
         head_dim=128, causal=True, causal_align="klens", k_lens=np.array([3000, 1700, 0], dtype=np.int32),
         head_sink=np.array([0.5, -1.0, 2.0, 0.0], dtype=np.float32)), 5),
+    # head_dim 64, not causal, key lengths that end some ranges early and leave others empty (their
+    # first K and V tiles are copied at kernel entry and must be waited for), a ragged key axis
+    "klens_ragged_d64": lambda: wl.make_case(
+        name="splitkl", seed=2206, dtype="bf16", layout="bshd", batch=3, heads=4, kv_heads=2, q_len=64, k_len=5000,
+        head_dim=64, k_lens=np.array([5000, 2000, 1], dtype=np.int32)),
     # float32 on the CUDA-core path, 3 forced ranges
     "f32_generic": lambda: _with_ranges(wl.make_case(
         name="split32", seed=2205, dtype="f32", batch=1, heads=2, q_len=40, k_len=700, head_dim=32, causal=True), 3),
