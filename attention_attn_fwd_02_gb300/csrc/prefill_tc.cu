@@ -67,6 +67,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
   int lo_u, hi_u;
+  int last_live;   // a broadcast mask's last key with a value other than -inf in the CTA's span
 };
 
 template <int D>
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
     sb.lo_u = 0x7fffffff;
     sb.hi_u = -1;
+    sb.last_live = -1;
     sb.abort = 0;
     mbar_init(&sb.q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
@@ -223,6 +225,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     lo_u = sb.lo_u;
     hi_u = sb.hi_u;
+  }
+  // A broadcast mask whose last keys are -inf throughout (key padding) ends
+  // the CTA's key span at its last key with another value: the tiles after
+  // it would hold only -inf scores.  Only the end moves (the first tile's
+  // copies may already be on their way); NaN and +inf entries count as keys
+  // with a value (they make rows NaN).  Spans up to kTrimSpan keys.
+  constexpr int kTrimSpan = 4096;
+  if (MASK && mask_bcast && hi_u > lo_u && hi_u - lo_u <= kTrimSpan) {
+    const float* mr = p.M + p.m.off + (int64_t)b * p.m.bs;
+    constexpr int kPer = (kTrimSpan + kThreads - 1) / kThreads;
+    float mv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int k = lo_u + (int)threadIdx.x + j * kThreads;
+      mv[j] = k < hi_u ? __ldg(mr + k) : -INFINITY;
+    }
+    int last = -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (!(mv[j] == -INFINITY)) last = lo_u + (int)threadIdx.x + j * kThreads;
+    last = __reduce_max_sync(0xffffffffu, last);
+    if (lane == 0 && last >= 0) atomicMax(&sb.last_live, last);
+    __syncthreads();
+    hi_u = max(sb.last_live + 1, lo_u);   // lo_u: no key with a value, nothing to compute
+    hi_0 = min(hi_0, hi_u);
   }
   const uint32_t tmem = sb.tmem_base;
   const bool any = hi_u > lo_u;
