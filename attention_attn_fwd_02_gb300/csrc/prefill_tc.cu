@@ -102,7 +102,7 @@ template <int D, bool BF16, bool MASK, bool XF>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const Problem p, const int n_qblocks,
-                      const int mask_bcast, const int drop_first_copy, const Split sp) {
+                      const int pair_heads, const int mask_bcast, const int drop_first_copy, const Split sp) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,11 +126,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int blk = sp.n_splits > 1 ? (int)(blockIdx.x / sp.n_splits) : (int)blockIdx.x;
   const int64_t kr0 = sp.n_splits > 1 ? (int64_t)(blockIdx.x % sp.n_splits) * sp.split_len : 0;
   const int64_t kr1 = sp.n_splits > 1 ? min((int64_t)p.Sk, kr0 + sp.split_len) : (int64_t)p.Sk;
-  const int hb = lpt ? blk % HB : blk / n_qblocks;
-  const int qb = lpt ? n_qblocks - 1 - blk / HB : blk % n_qblocks;
-  const int h = hb % p.H, b = hb / p.H;
-  const int g = h / p.qpg;
-  const int q0 = qb * 2 * BM;
+  // The two query tiles are rows [q0, q0 + 256) of one head, or with
+  // pair_heads (q_len <= 128 and at least two query heads a kv head) rows
+  // [0, q_len) of two query heads of one kv head, which then share every K
+  // and V tile instead of one tile holding no row.
+  int h, b, g, q0;
+  if (pair_heads) {
+    const int npg = (p.qpg + 1) / 2;
+    const int pr = blk % npg;
+    g = (blk / npg) % p.G;
+    b = blk / (npg * p.G);
+    h = g * p.qpg + 2 * pr;
+    q0 = 0;
+  } else {
+    const int hb = lpt ? blk % HB : blk / n_qblocks;
+    const int qb = lpt ? n_qblocks - 1 - blk / HB : blk % n_qblocks;
+    h = hb % p.H;
+    b = hb / p.H;
+    g = h / p.qpg;
+    q0 = qb * 2 * BM;
+  }
+  const int ht_step = pair_heads ? 1 : 0;    // query tile 1: head h + ht_step,
+  const int rt_step = pair_heads ? 0 : BM;   // rows from q0 + rt_step
   // Without a window or segment starts every row's keys start at the key
   // range's start (kr0, a multiple of BN), so the CTA's first K and V tiles
   // are known before any key length is read from global memory: their copies
@@ -165,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_expect_tx(&sb.q_full, 2 * C::kQTile);
     for (int tt = 0; tt < 2; ++tt)
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * BM, h, b);
+        tma_load_4d(q_s + tt * C::kQTile + c * BM * 128, &tm_q, &sb.q_full, c * 64, q0 + tt * rt_step,
+                    h + tt * ht_step, b);
     if (early) {
       const int krow = (int)kr0;
       mbar_expect_tx(&sb.k_full[0], C::kKTile);
@@ -179,9 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- row ranges and their union ----
   const int t = warp / 4;                       // query tile of a softmax thread
   const int r = (warp % 4) * 32 + lane;         // row within the tile = TMEM lane
-  const int qrow = q0 + t * BM + r;
+  const int qrow = q0 + t * rt_step + r;
+  // (pair_heads with an odd count of query heads: tile 1 may have no head)
   int lo = 0, hi = 0;
-  if (warp < 8 && qrow < p.Sq) {
+  if (warp < 8 && qrow < p.Sq && h + t * ht_step < (g + 1) * p.qpg) {
     int64_t lo64, hi64;
     row_range(p, b, qrow, lo64, hi64);
     lo64 = max(lo64, kr0);
@@ -434,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t scale2 = f2u(p.scale, p.scale);
     const float* mrow = nullptr;
     if (MASK && qrow < p.Sq)
-      mrow = p.M + p.m.off + (int64_t)b * p.m.bs + (int64_t)h * p.m.hs + (int64_t)qrow * p.m.rs;
+      mrow = p.M + p.m.off + (int64_t)b * p.m.bs + (int64_t)(h + t * ht_step) * p.m.hs + (int64_t)qrow * p.m.rs;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     uint32_t x[BN];
@@ -632,13 +651,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n_my > 0) ok = wait_warp(&sb.o_done[t], (uint32_t)(n_my - 1) & 1u, &sb.abort, p.status);
     if (ok) {
       fence_after();
-      const bool valid = qrow < p.Sq;
+      const int ht = h + t * ht_step;   // this thread's query head
+      const bool valid = qrow < p.Sq && ht < (g + 1) * p.qpg;
       // The sink logit joins the denominator (and rescales the accumulated O);
       // with key ranges the merge adds it once.
-      const float o_mul = p.sink_on && sp.n_splits == 1 ? fold_sink<true>(m_ref, l, sink_logit(p, h) * kLog2e) : 1.f;
+      const float o_mul = p.sink_on && sp.n_splits == 1 ? fold_sink<true>(m_ref, l, sink_logit(p, ht) * kLog2e) : 1.f;
       const bool hidden_row = (l == 0.f);         // no visible key; a NaN l stays a NaN row
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      T* orow = valid ? static_cast<T*>(p.O) + p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs +
+      T* orow = valid ? static_cast<T*>(p.O) + p.o.off + (int64_t)b * p.o.bs + (int64_t)ht * p.o.hs +
                             (int64_t)qrow * p.o.rs
                       : nullptr;
       const float inv = o_mul / l;
@@ -647,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // This key range's partial: O / l in float32 and its LSE (-inf when
         // the range has no visible key; the merge then gives it no weight).
         const int split = (int)(blockIdx.x % sp.n_splits);
-        const int64_t prow = ((int64_t)b * p.H + h) * p.Sq + qrow;
+        const int64_t prow = ((int64_t)b * p.H + ht) * p.Sq + qrow;
         float4* po = reinterpret_cast<float4*>(sp.part_o + (prow * sp.n_splits + split) * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -689,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (valid && p.lse)
-          p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + qrow] =
+          p.lse[(int64_t)b * p.lse_bs + (int64_t)ht * p.lse_hs + qrow] =
               hidden_row ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
       }
     }
@@ -713,7 +733,10 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
       !tma_map_bhsd(&mv, p.V, p.dtype, D, p.Sk, p.G, p.B, p.v, BN))
     return -1;  // not describable: caller falls back
   const int nqb = (p.Sq + 2 * BM - 1) / (2 * BM);
-  const int64_t blocks = (int64_t)nqb * p.H * p.B * sp.n_splits;
+  // q_len <= 128 with two or more query heads a kv head: a CTA takes two
+  // heads (one query tile each) of one kv head.
+  const int pair = (p.Sq <= BM && p.qpg >= 2) ? 1 : 0;
+  const int64_t blocks = (pair ? (int64_t)p.B * p.G * ((p.qpg + 1) / 2) : (int64_t)nqb * p.H * p.B) * sp.n_splits;
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D>::kSmem + 1024;
   auto kern = prefill_tc_kernel<D, BF16, MASK, XF>;
@@ -735,7 +758,7 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
                              ? 1
                              : 0;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, mask_bcast, drop, sp);
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, p, nqb, pair, mask_bcast, drop, sp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -380,6 +380,33 @@ def test_softcap_and_sink(i):
     assert st["nan_rows"] == 0      # with a sink a row without keys gives O = 0, not NaN
 
 
+PAIRED = [
+    # dtype, B, H, G, Sq, Sk, D, causal offset (None: not causal), mask kind, sink: q_len <= 128 with two or
+    # more query heads a kv head, so a CTA takes two heads of one kv head (one query tile each)
+    ("bf16", 2, 6, 2, 100, 700, 128, 600, "bhqk", True),    # three heads a group: the last pair has one
+    ("f16", 1, 8, 2, 128, 1000, 64, None, "b11k", False),    # q_len exactly one tile, staged mask
+    ("bf16", 3, 4, 2, 1, 300, 128, None, None, True),        # one query row, key lengths below
+    ("bf16", 1, 4, 1, 129, 400, 64, 0, None, False),         # q_len 129: two tiles of one head (not paired)
+]
+
+
+@pytest.mark.parametrize("i", range(len(PAIRED)))
+def test_paired_query_heads(i):
+    dtype, B, H, G, Sq, Sk, D, off, mk, sink = PAIRED[i]
+    r = np.random.default_rng(1500 + i)
+    mask = None
+    if mk is not None:
+        shape = {"bhqk": (B, H, Sq, Sk), "b11k": (B, 1, 1, Sk)}[mk]
+        mask = r.standard_normal(shape).astype(np.float32)
+        mask[r.random(shape) < 0.1] = -np.inf
+    k_lens = r.integers(1, Sk + 1, size=B).astype(np.int32)
+    head_sink = (r.standard_normal(H) * 2).astype(np.float32) if sink else None
+    c = wl.make_case(name=f"pair{i}", seed=1550 + i, dtype=dtype, layout="bshd", batch=B, heads=H, kv_heads=G,
+                     q_len=Sq, k_len=Sk, head_dim=D, causal=off is not None, causal_offset=off, mask=mask,
+                     mask_kind=mk or "b11k", k_lens=k_lens, head_sink=head_sink)
+    run_and_compare(c)
+
+
 NEG_SCALE = [
     # head_dim, mask, segment starts: the transformed-score instantiations of the
     # tensor-core kernels without a softcap (a scale that is not positive)
