@@ -133,7 +133,8 @@ template <int D, bool BF16, bool MASK, bool XF>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                       const Problem p, const int n_qblocks, const int drop_first_copy, const int mask_stage,
+                       const Problem p, const int n_qblocks, const int pair_heads, const int drop_first_copy,
+                       const int mask_stage,
                        const int o_tma, const Split sp) {
   using C = Cfg<D, MASK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -154,12 +155,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int blk = sp.n_splits > 1 ? pair / sp.n_splits : pair;
   const int64_t kr0 = sp.n_splits > 1 ? (int64_t)(pair % sp.n_splits) * sp.split_len : 0;
   const int64_t kr1 = sp.n_splits > 1 ? min((int64_t)p.Sk, kr0 + sp.split_len) : (int64_t)p.Sk;
-  const int hb = lpt ? blk % HB : blk / n_qblocks;
-  const int qb = lpt ? n_qblocks - 1 - blk / HB : blk % n_qblocks;
-  const int h = hb % p.H, b = hb / p.H;
-  const int g = h / p.qpg;
-  const int qp0 = qb * 2 * BM;              // the pair's first row
-  const int q0 = qp0 + (int)rank * BM;      // this CTA's first row
+  // The pair's CTAs hold rows [qp0, qp0 + 128) and [qp0 + 128, qp0 + 256) of
+  // one head, or with pair_heads (q_len <= 128 and at least two query heads a
+  // kv head) rows [0, q_len) of two query heads of one kv head, which then
+  // share every K and V tile instead of the follower holding no row.
+  int h, b, g, qp0, q0;
+  if (pair_heads) {
+    const int npg = (p.qpg + 1) / 2;
+    const int pr = blk % npg;
+    g = (blk / npg) % p.G;
+    b = blk / (npg * p.G);
+    h = g * p.qpg + 2 * pr + (int)rank;     // this CTA's head
+    qp0 = 0;
+    q0 = 0;
+  } else {
+    const int hb = lpt ? blk % HB : blk / n_qblocks;
+    const int qb = lpt ? n_qblocks - 1 - blk / HB : blk % n_qblocks;
+    h = hb % p.H;
+    b = hb / p.H;
+    g = h / p.qpg;
+    qp0 = qb * 2 * BM;                       // the pair's first row
+    q0 = qp0 + (int)rank * BM;               // this CTA's first row
+  }
+  // (pair_heads with an odd count of query heads: the follower of a group's
+  // last pair has no head; it computes along and writes nothing)
+  const bool head_ok = h < (g + 1) * p.qpg;
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tm_q);
@@ -662,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     l = sb.red_l[0][r] + sb.red_l[1][r];
     if (ok) {
       fence_after();
-      const bool valid = qrow < p.Sq;
+      const bool valid = qrow < p.Sq && head_ok;
       // The sink logit joins the denominator (and rescales the accumulated O);
       // with key ranges the merge adds it once.
       const float o_mul = p.sink_on && sp.n_splits == 1 ? fold_sink<true>(m_ref, l, sink_logit(p, h) * kLog2e) : 1.f;
@@ -736,7 +756,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (o_tma) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0 && q0 + wr0 < p.Sq) {
+          if (lane == 0 && q0 + wr0 < p.Sq && head_ok) {
             for (int cc = 0; cc < 2; ++cc)
               tma_store_4d(&tm_o, ring + (ch * 2 + cc) * (BM * 128) + wr0 * 128, (ch * 2 + cc) * 64, q0 + wr0, h, b);
             bulk_store_commit_wait_read();
@@ -772,7 +792,11 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   const int o_tma = sp.n_splits == 1 && tma_map_bhsd(&mo, p.O, p.dtype, D, p.Sq, p.H, p.B, p.o, 32) ? 1 : 0;
   if (!o_tma) memset(&mo, 0, sizeof mo);
   const int npq = (p.Sq + 2 * BM - 1) / (2 * BM);   // pairs per (batch, head)
-  const int64_t blocks = 2 * (int64_t)npq * p.H * p.B * sp.n_splits;
+  // q_len <= 128 with two or more query heads a kv head: a pair takes two
+  // heads of one kv head (one CTA each).
+  const int ph = (p.Sq <= BM && p.qpg >= 2) ? 1 : 0;
+  const int64_t blocks =
+      2 * (ph ? (int64_t)p.B * p.G * ((p.qpg + 1) / 2) : (int64_t)npq * p.H * p.B) * sp.n_splits;
   if (blocks > 0x7fffffff) return -1;
   const int smem = Cfg<D, MASK>::kSmem + 1024;
   auto kern = prefill_tc2_kernel<D, BF16, MASK, XF>;
@@ -780,7 +804,7 @@ int launch(const Problem& p, const Split& sp, cudaStream_t st) {
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   const int drop = take_injection() == ATTN_INJECT_DROP_FIRST_COPY ? 1 : 0;
   const int mask_stage = (MASK && p.m.hs == 0 && p.m.rs == 0) ? 1 : 0;
-  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, mo, p, npq, drop, mask_stage, o_tma, sp);
+  kern<<<(unsigned)blocks, kThreads, smem, st>>>(mq, mk, mv, mo, p, npq, ph, drop, mask_stage, o_tma, sp);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -387,6 +387,8 @@ PAIRED = [
     ("f16", 1, 8, 2, 128, 1000, 64, None, "b11k", False),    # q_len exactly one tile, staged mask
     ("bf16", 3, 4, 2, 1, 300, 128, None, None, True),        # one query row, key lengths below
     ("bf16", 1, 4, 1, 129, 400, 64, 0, None, False),         # q_len 129: two tiles of one head (not paired)
+    ("f16", 2, 6, 2, 100, 700, 256, 600, "bhqk", True),     # head_dim 256: the CTA pair takes two heads; odd count
+    ("bf16", 1, 4, 2, 128, 300, 256, None, "b11k", False),   # head_dim 256, staged mask
 ]
 
 
