@@ -67,7 +67,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
   int lo_u, hi_u;
-  int last_live;   // a broadcast mask's last key with a value other than -inf in the CTA's span
+  int first_live, last_live;   // a broadcast mask's first / last key with a value other than -inf in the CTA's span
 };
 
 template <int D>
@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // are known before any key length is read from global memory: their copies
   // start at once, with Q's, into stage 0.  (Not with the test hook, which
   // drops the producer's first K copy.)
-  const bool early = !(p.causal && p.window >= 0) && p.seg == nullptr && !(drop_first_copy && blockIdx.x == 0);
+  // (Nor with a staged broadcast mask, whose -inf keys can move the first tile.)
+  const bool early = !(p.causal && p.window >= 0) && p.seg == nullptr && !(drop_first_copy && blockIdx.x == 0) &&
+                     !(MASK && mask_bcast);
 
   if (threadIdx.x == 0) {
     // The copies' descriptors start on their way before anything else.
@@ -162,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
     sb.lo_u = 0x7fffffff;
     sb.hi_u = -1;
+    sb.first_live = 0x7fffffff;
     sb.last_live = -1;
     sb.abort = 0;
     mbar_init(&sb.q_full, 1);
@@ -245,11 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     lo_u = sb.lo_u;
     hi_u = sb.hi_u;
   }
-  // A broadcast mask whose last keys are -inf throughout (key padding) ends
-  // the CTA's key span at its last key with another value: the tiles after
-  // it would hold only -inf scores.  Only the end moves (the first tile's
-  // copies may already be on their way); NaN and +inf entries count as keys
-  // with a value (they make rows NaN).  Spans up to kTrimSpan keys.
+  // A broadcast mask whose first or last keys are -inf throughout (key
+  // padding, left or right) starts and ends the CTA's key span at its first
+  // and last keys with another value: the tiles outside would hold only -inf
+  // scores.  NaN and +inf entries count as keys with a value (they make rows
+  // NaN).  Spans up to kTrimSpan keys.
   constexpr int kTrimSpan = 4096;
   if (MASK && mask_bcast && hi_u > lo_u && hi_u - lo_u <= kTrimSpan) {
     const float* mr = p.M + p.m.off + (int64_t)b * p.m.bs;
@@ -260,14 +263,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k = lo_u + (int)threadIdx.x + j * kThreads;
       mv[j] = k < hi_u ? __ldg(mr + k) : -INFINITY;
     }
-    int last = -1;
+    int first = 0x7fffffff, last = -1;
 #pragma unroll
     for (int j = 0; j < kPer; ++j)
-      if (!(mv[j] == -INFINITY)) last = lo_u + (int)threadIdx.x + j * kThreads;
+      if (!(mv[j] == -INFINITY)) {
+        const int k = lo_u + (int)threadIdx.x + j * kThreads;
+        first = min(first, k);
+        last = k;
+      }
+    first = __reduce_min_sync(0xffffffffu, first);
     last = __reduce_max_sync(0xffffffffu, last);
-    if (lane == 0 && last >= 0) atomicMax(&sb.last_live, last);
+    if (lane == 0 && last >= 0) {
+      atomicMin(&sb.first_live, first);
+      atomicMax(&sb.last_live, last);
+    }
     __syncthreads();
-    hi_u = max(sb.last_live + 1, lo_u);   // lo_u: no key with a value, nothing to compute
+    if (sb.last_live >= 0) {
+      lo_u = sb.first_live;
+      hi_u = sb.last_live + 1;
+    } else {
+      hi_u = lo_u;   // no key with a value: nothing to compute
+    }
     hi_0 = min(hi_0, hi_u);
   }
   const uint32_t tmem = sb.tmem_base;

@@ -252,18 +252,22 @@ def test_staged_broadcast_mask_batches_and_special_values(i):
 
 
 @pytest.mark.parametrize("D,causal", [(128, False), (64, True)])
-def test_trailing_masked_keys_end_the_key_span(D, causal):
-    """A staged [B,1,1,K] mask whose last keys are -inf (key padding) ends a
-    CTA's key tiles at its last key with another value: entry 0 is padded
-    from key 500; entry 1 from key 300 except a NaN at key 600 (which keeps its
-    tile: the rows that see it are NaN); entry 2 is -inf throughout (fully
-    hidden rows, LSE -inf).  Against the oracle, in both MaskedRows modes."""
-    B, H, Sq, Sk = 3, 4, 300, 708
+def test_padded_masked_keys_bound_the_key_span(D, causal):
+    """A staged [B,1,1,K] mask whose first or last keys are -inf (key padding)
+    starts and ends a CTA's key tiles at its first and last keys with another
+    value: entry 0 is padded from key 500; entry 1 from key 300 except a NaN at
+    key 600 (which keeps its tile: the rows that see it are NaN); entry 2 is
+    -inf throughout (fully hidden rows, LSE -inf); entry 3 is padded below key
+    400 and from key 650 (under the causal bound its first rows see no key).
+    Against the oracle, in both MaskedRows modes."""
+    B, H, Sq, Sk = 4, 4, 300, 708
     mask = np.random.default_rng(1950 + D).standard_normal((B, 1, 1, Sk)).astype(np.float32)
     mask[0, 0, 0, 500:] = -np.inf
     mask[1, 0, 0, 300:] = -np.inf
     mask[1, 0, 0, 600] = np.nan
     mask[2] = -np.inf
+    mask[3, 0, 0, :400] = -np.inf
+    mask[3, 0, 0, 650:] = -np.inf
     for mr in ("nan", "zero"):
         c = wl.make_case(name=f"trim{D}{mr}", seed=1960 + D, dtype="bf16", layout="bhsd", batch=B, heads=H,
                          kv_heads=2, q_len=Sq, k_len=Sk, head_dim=D, mask=mask, mask_kind="b11k", masked_rows=mr,
