@@ -660,8 +660,8 @@ def extra_cases(pk, pk_kind):
         d = {"workload": case.name, "ms_median": med, "ms_min": mn}
         d.update(case_line(case, med, pk, pk_kind))
         if small:
-            # The small workloads also by the survey's method for them: back-to-back
-            # calls with L2 left warm (median of 200), beside the flushed figure.
+            # The small (latency-bound) workloads also as back-to-back calls with
+            # L2 left warm (median of 200), beside the flushed figure.
             med_w, _ = time_case(case, 200, 5, flush=False, lead_us=100)
             w = case_line(case, med_w, pk, pk_kind)
             d["warm_l2_back_to_back"] = {"ms_median": med_w, "value": w["value"], "frac": w.get("frac")}
