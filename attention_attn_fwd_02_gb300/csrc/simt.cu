@@ -13,7 +13,11 @@
 //
 // Layout of the work: a CTA of 128 threads owns 128/TPR query rows of one
 // (batch, kv head) pair; TPR threads (4 to 32) share a row, each holding up to
-// 8 of its head_dim elements (element d lives in lane d % TPR, slot d / TPR).  Rows are
+// 8 of its head_dim elements (element d lives in lane d % TPR, slot d / TPR;
+// when head_dim is exactly 8 * TPR, a float32 problem takes a form in which a
+// lane holds the two 4-element chunks lr and lr + TPR of the row, read from
+// shared memory as one 16-byte load each: a quarter of the load instructions
+// and no per-slot bounds tests).  Rows are
 // ordered (query, head-in-group), so the heads that share a key/value head
 // read each staged key tile once.  Dot products are reduced over the TPR lanes
 // with an xor butterfly, which gives every lane the same bits; every sum has a
@@ -21,6 +25,8 @@
 #include <float.h>
 #include <limits.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -38,10 +44,10 @@ constexpr int kTile = 32;    // keys per staged tile
 // float32 problem 15.0 -> 13.0 us a call against three CTAs' 168 registers,
 // larger problems 10-15 % slower than with three, still 1.1-1.4x faster than
 // the per-key branching form).
-template <typename T, int TPR, bool KV8>
+template <typename T, int TPR, bool KV8, bool FULL>
 __global__ void __launch_bounds__(kThreads, 2) simt_attn_kernel(Problem p, Split sp, int64_t row_blocks) {
   constexpr int RPC = kThreads / TPR;  // rows per CTA
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   float* Ks = smem;
   float* Vs = smem + kTile * p.D;
   __shared__ int s_lo, s_hi;
@@ -65,6 +71,9 @@ __global__ void __launch_bounds__(kThreads, 2) simt_attn_kernel(Problem p, Split
   const int64_t k0 = (int64_t)split * sp.split_len;
   const int64_t k1 = min((int64_t)p.Sk, k0 + (int64_t)sp.split_len);
   const int rl = threadIdx.x / TPR, lr = threadIdx.x % TPR;
+  // The head_dim element in slot s of this lane, and whether it exists.
+  auto dim_of = [&](int s) { return FULL ? 4 * (lr + TPR * (s / 4)) + s % 4 : lr + TPR * s; };
+  auto has = [&](int s) { return FULL || (TPR * s < D && lr + TPR * s < D); };
   const int64_t r = (int64_t)rb * RPC + rl;
   const bool valid = r < (int64_t)p.Sq * p.qpg;
   const int i = valid ? (int)(r / p.qpg) : 0;
@@ -100,8 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2) simt_attn_kernel(Problem p, Split
   float qr[kSlots], acc[kSlots];
 #pragma unroll
   for (int s = 0; s < kSlots; ++s) {
-    const int d = lr + TPR * s;
-    qr[s] = (valid && d < D) ? to_f32(Q[qb + d]) : 0.f;
+    qr[s] = (valid && has(s)) ? to_f32(Q[qb + dim_of(s)]) : 0.f;
     acc[s] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -150,10 +158,16 @@ __global__ void __launch_bounds__(kThreads, 2) simt_attn_kernel(Problem p, Split
 #pragma unroll
     for (int j = 0; j < kTile; ++j) {
       float part = 0.f;
+      if constexpr (FULL) {
+        const float4* kr = reinterpret_cast<const float4*>(Ks + j * D);
+        const float4 a = kr[lr], c = kr[lr + TPR];
+        const float kx[kSlots] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-      for (int s = 0; s < kSlots; ++s) {
-        const int d = lr + TPR * s;
-        if (TPR * s < D && d < D) part = fmaf(qr[s], Ks[j * D + d], part);
+        for (int s = 0; s < kSlots; ++s) part = fmaf(qr[s], kx[s], part);
+      } else {
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s)
+          if (has(s)) part = fmaf(qr[s], Ks[j * D + dim_of(s)], part);
       }
 #pragma unroll
       for (int off = TPR / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
@@ -188,14 +202,30 @@ __global__ void __launch_bounds__(kThreads, 2) simt_attn_kernel(Problem p, Split
       lt += sc[j];
     }
     l = fmaf(l, corr, lt);
+    if constexpr (FULL) {
+      float t[kSlots];
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
-      const int d = lr + TPR * s;
-      if (TPR * s < D && d < D) {
-        float t = 0.f;
+      for (int s = 0; s < kSlots; ++s) t[s] = 0.f;
 #pragma unroll
-        for (int j = 0; j < kTile; ++j) t = fmaf(sc[j], Vs[j * D + d], t);
-        acc[s] = fmaf(acc[s], corr, t);
+      for (int j = 0; j < kTile; ++j) {
+        const float4* vr = reinterpret_cast<const float4*>(Vs + j * D);
+        const float4 a = vr[lr], c = vr[lr + TPR];
+        const float vx[kSlots] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) t[s] = fmaf(sc[j], vx[s], t[s]);
+      }
+#pragma unroll
+      for (int s = 0; s < kSlots; ++s) acc[s] = fmaf(acc[s], corr, t[s]);
+    } else {
+#pragma unroll
+      for (int s = 0; s < kSlots; ++s) {
+        if (has(s)) {
+          const int d = dim_of(s);
+          float t = 0.f;
+#pragma unroll
+          for (int j = 0; j < kTile; ++j) t = fmaf(sc[j], Vs[j * D + d], t);
+          acc[s] = fmaf(acc[s], corr, t);
+        }
       }
     }
     m = m_new;
@@ -216,20 +246,16 @@ __global__ void __launch_bounds__(kThreads, 2) simt_attn_kernel(Problem p, Split
     const int64_t ob = p.o.off + (int64_t)b * p.o.bs + (int64_t)h * p.o.hs + (int64_t)i * p.o.rs;
     const float fill = p.masked_zero ? 0.f : NAN;
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
-      const int d = lr + TPR * s;
-      if (TPR * s < D && d < D) O[ob + d] = from_f32<T>(hidden ? fill : acc[s] / l);
-    }
+    for (int s = 0; s < kSlots; ++s)
+      if (has(s)) O[ob + dim_of(s)] = from_f32<T>(hidden ? fill : acc[s] / l);
     if (p.lse && lr == 0)
       p.lse[(int64_t)b * p.lse_bs + (int64_t)h * p.lse_hs + i] = hidden ? -INFINITY : m + logf(l);
   } else {
     const int64_t row = ((int64_t)b * p.H + h) * p.Sq + i;
     float* po = sp.part_o + (row * sp.n_splits + split) * D;
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
-      const int d = lr + TPR * s;
-      if (TPR * s < D && d < D) po[d] = hidden ? 0.f : acc[s] / l;
-    }
+    for (int s = 0; s < kSlots; ++s)
+      if (has(s)) po[dim_of(s)] = hidden ? 0.f : acc[s] / l;
     if (lr == 0) sp.part_lse[row * sp.n_splits + split] = hidden ? -INFINITY : m + logf(l);
   }
 }
@@ -313,8 +339,8 @@ __global__ void __launch_bounds__(128) combine_kernel(int n_splits, int64_t rows
         bad ? NAN : (M == -INFINITY ? -INFINITY : M + logf(ws));
 }
 
-template <typename T, int TPR, bool KV8>
-cudaError_t launch_simt_t(const Problem& p, const Split& s, cudaStream_t st) {
+template <typename T, int TPR, bool KV8, bool FULL>
+cudaError_t launch_simt_f(const Problem& p, const Split& s, cudaStream_t st) {
   constexpr int RPC = kThreads / TPR;
   const int64_t rows = (int64_t)p.Sq * p.qpg;
   const int64_t row_blocks = (rows + RPC - 1) / RPC;
@@ -322,10 +348,20 @@ cudaError_t launch_simt_t(const Problem& p, const Split& s, cudaStream_t st) {
   if (blocks <= 0) return cudaSuccess;
   if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)2 * kTile * p.D * sizeof(float);
-  cudaError_t e = ensure_smem((const void*)simt_attn_kernel<T, TPR, KV8>, (int)smem);
+  cudaError_t e = ensure_smem((const void*)simt_attn_kernel<T, TPR, KV8, FULL>, (int)smem);
   if (e != cudaSuccess) return e;
-  simt_attn_kernel<T, TPR, KV8><<<(unsigned)blocks, kThreads, smem, st>>>(p, s, row_blocks);
+  simt_attn_kernel<T, TPR, KV8, FULL><<<(unsigned)blocks, kThreads, smem, st>>>(p, s, row_blocks);
   return cudaGetLastError();
+}
+
+// The chunked form only for float32 values (the exact path's own dtype); the
+// half and int8 forms stay on the general layout.
+template <typename T, int TPR, bool KV8>
+cudaError_t launch_simt_t(const Problem& p, const Split& s, cudaStream_t st) {
+  if constexpr (!KV8 && std::is_same<T, float>::value) {
+    if (p.D == kSlots * TPR) return launch_simt_f<T, TPR, KV8, true>(p, s, st);
+  }
+  return launch_simt_f<T, TPR, KV8, false>(p, s, st);
 }
 
 template <typename T, bool KV8>
