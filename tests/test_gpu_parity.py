@@ -94,6 +94,8 @@ EDGE = [
     ("f32", "bhsd", 2, 4, 2, 70, 150, 64, True, None, True, True, "bhqk", "nan", False),
     ("f32", "bshd", 1, 2, 1, 1, 300, 128, False, None, False, True, "b11k", "zero", False),
     ("f32", "bshd", 2, 3, 3, 40, 33, 32, True, 2, False, False, "11qk", "nan", False),
+    ("bf16", "bhsd", 2, 4, 2, 70, 90, 32, True, None, True, True, "bhqk", "nan", False),
+    ("f16", "bshd", 1, 4, 1, 1, 200, 32, False, None, False, True, "b11k", "zero", False),
     # head_dim 256 with two and three key tiles: the last P V may still be two phases behind
     ("bf16", "bhsd", 2, 4, 2, 200, 100, 256, False, None, False, False, None, "nan", False),
     ("f16", "bshd", 1, 3, 1, 260, 190, 256, True, None, False, True, None, "zero", False),
